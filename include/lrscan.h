@@ -1,0 +1,205 @@
+/*
+ * lrscan.h -- C ABI of the GB300 (sm_103a) gated linear-recurrence scan
+ * library.  Forward-only; one GPU; the kernels are hand-written CUDA.
+ *
+ * Every scan computes a recurrence  h_t = a_t (.) h_{t-1} + b_t  with a
+ * readout, over post-projection, post-activation inputs, starting from an
+ * optional initial state and returning the outputs and the final state.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [SSM]   cortexnet 3.2.1 wheel, cortexnet/ssm.py -- module docstring (ZOH
+ *           discretisation), MultiScaleSSM.__init__ (multi-scale A_log, D),
+ *           MultiScaleSSM.forward (A = -exp(A_log), dt = softplus(dt_proj(x)),
+ *           D skip, silu(z) gate, past_state / new_state),
+ *           MultiScaleSSM._selective_scan (the recurrence, in float32).
+ *   [RGLRU] lrnnx docs, lrnnx.models.ltv.rglru module source -- RGLRU.forward
+ *           (gates, rglru_scan_fn(u, delta, a, return_last_state)) and
+ *           RGLRU.step (fallback update a^(c r), sqrt(1 - a^2)).
+ *   [HGRN2] frankenstein-transformer docs, HGRN2 Attention page --
+ *           S_t = diag(g_t) S_{t-1} + v_t k_t^T, per-head matrix state,
+ *           lower-bounded forget gate, hidden % heads check.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or retains them.  Every tensor is dense and
+ *    row-major (last index fastest) in the layout written beside it.  A
+ *    required pointer may be NULL only when its tensor has no elements.
+ *  - Each tensor's base address must be 16-byte aligned (LR_ERR_MISALIGNED).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Argument errors are returned synchronously and launch
+ *    nothing.  A failed launch returns LR_ERR_CUDA.
+ *  - Errors detected on the device (a bounded wait that ran out) set a
+ *    device-wide sticky status; lr_check_status() reads and clears it.
+ *  - State and arithmetic are float32 whatever the I/O dtype; bf16 outputs
+ *    are rounded once, at the store.  There is no CPU fallback.
+ *  - `workspace` is caller-owned device scratch of at least the size the
+ *    matching *_workspace_size() call returns for the same sizes on the
+ *    current device (0 bytes is possible; then workspace may be NULL).  Its
+ *    contents need no initialisation.  Calls that overlap in time must use
+ *    distinct workspaces.
+ */
+#ifndef LRSCAN_H
+#define LRSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA
+ * headers. */
+typedef struct CUstream_st *lr_stream_t;
+
+/* I/O element type of the activation tensors. */
+typedef enum { LR_F32 = 0, LR_BF16 = 1 } lr_dtype;
+
+/* Status codes (0 = success, negative = error). */
+enum {
+    LR_OK = 0,
+    LR_ERR_INVALID_ARG = -1,  /* NULL required pointer, negative size, bad scalar */
+    LR_ERR_UNSUPPORTED = -2,  /* legal but unsupported shape or dtype */
+    LR_ERR_MISALIGNED = -3,   /* a tensor base is not 16-byte aligned */
+    LR_ERR_WORKSPACE = -4,    /* workspace NULL or smaller than required */
+    LR_ERR_CUDA = -5,         /* a CUDA runtime/driver call failed */
+    LR_ERR_TIMEOUT = -6,      /* device side: a bounded wait ran out */
+    LR_ERR_RANGE = -7         /* device side: HGRN2 chunk log-gate spread too wide */
+};
+
+/* Human-readable name of a status code (static storage). */
+const char *lr_status_string(int code);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int lr_version(void);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side sticky
+ * status of the current device (LR_OK when no kernel reported an error).
+ */
+int lr_check_status(lr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Selective SSM scan                                                        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [SSM] MultiScaleSSM._selective_scan + the D skip and silu(z) gate of
+ * MultiScaleSSM.forward.  For every batch b and channel d, with the state
+ * h[n] = h0[b,d,n] (zero when h0 == NULL) and A[n] = -exp(A_log[d,n]):
+ *
+ *   delta_t = dt_softplus ? softplus(dt[b,t,d]) : dt[b,t,d]
+ *             (softplus as torch: identity above 20, else log(1 + e^x))
+ *   h[n]    = exp(delta_t * A[n]) * h[n] + delta_t * Bm[b,t,n] * x[b,t,d]
+ *   y[b,t,d] = (sum_n Cm[b,t,n] h[n] + Dskip[d] x[b,t,d]) * silu(z[b,t,d])
+ *
+ * and h_final[b,d,:] = h after the last step.  The readout uses the state
+ * after the update at t.  B_t and C_t are shared by all channels.
+ *
+ * Layouts: x, dt, z, y: (B, L, D) in `io`; Bm, Cm: (B, L, N) in `io`;
+ *          A_log: (D, N) fp32; Dskip: (D) fp32; h0, h_final: (B, D, N) fp32.
+ * Optional (NULL allowed): z (no gate), Dskip (no skip), h0 (zero state),
+ *          h_final (not written).
+ * Requirements: N == 16; D % 8 == 0 (bf16) or D % 4 == 0 (fp32), else
+ *          LR_ERR_UNSUPPORTED; delta >= 0 (a step size; with dt_softplus it
+ *          always is).  B, L may be 0 (nothing is launched; h_final = h0).
+ */
+size_t lr_selective_scan_workspace_size(int64_t B, int64_t L, int64_t D,
+                                        int64_t N, lr_dtype io);
+
+int lr_selective_scan_fwd(const void *x, const void *dt, const void *z,
+                          const void *Bm, const void *Cm,
+                          const float *A_log, const float *Dskip,
+                          const float *h0, void *y, float *h_final,
+                          int64_t B, int64_t L, int64_t D, int64_t N,
+                          lr_dtype io, int dt_softplus,
+                          void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* RG-LRU scalar-state scan                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [RGLRU] RGLRU.step fallback update applied at every step (the scan that
+ * rglru_scan_fn performs in RGLRU.forward).  For every b and channel d, with
+ * h = h0[b,d] (zero when NULL):
+ *
+ *   a_t = exp(c * r[b,t,d] * a_log[d])        (= a^(c r) with a = exp(a_log))
+ *   h   = a_t * h + sqrt(1 - a_t^2) * (i[b,t,d] * x[b,t,d])
+ *   y[b,t,d] = h
+ *
+ * and h_final[b,d] = h after the last step.  r and i are the recurrent and
+ * input gates after their sigmoid; c is the fixed gate scale (8 on the page).
+ *
+ * Layouts: x, r, i, y: (B, L, D) in `io`; a_log: (D) fp32 (<= 0);
+ *          h0, h_final: (B, D) fp32.  Optional: h0, h_final.
+ * Requirements: D % 8 == 0 (bf16) or D % 4 == 0 (fp32), else
+ *          LR_ERR_UNSUPPORTED; c finite.
+ */
+size_t lr_rglru_scan_workspace_size(int64_t B, int64_t L, int64_t D,
+                                    lr_dtype io);
+
+int lr_rglru_scan_fwd(const void *x, const void *r, const void *i,
+                      const float *a_log, float c, const float *h0,
+                      void *y, float *h_final,
+                      int64_t B, int64_t L, int64_t D, lr_dtype io,
+                      void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* HGRN2 matrix-state recurrence                                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [HGRN2] HGRN2Attention: per batch b and head h a dv x dk state S (row i =
+ * value channel, column j = key channel), S = S0[b,h] (zero when NULL):
+ *
+ *   S_t = diag(g_t) S_{t-1} + v_t k_t^T        (g_t scales the rows of S)
+ *   o_t = S_t q_t                              (after the update at t)
+ *
+ * and S_final[b,h] = S after the last step.  g is the forget gate after its
+ * activation and lower bound, in (0, 1].
+ *
+ * Layouts: q, k: (B, L, H*dk); v, g, o: (B, L, H*dv), all in `io`;
+ *          S0, S_final: (B, H, dv, dk) fp32.  Optional: S0, S_final.
+ * Requirements: H > 0; dk == dv == 128; chunk == 64; io == LR_BF16; else
+ *          LR_ERR_UNSUPPORTED.  Within every chunk of 64 steps the product
+ *          of a channel's gates must stay above e^-160 (always true when
+ *          g >= 0.09); otherwise the kernel sets LR_ERR_RANGE.
+ */
+size_t lr_hgrn2_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk,
+                               int64_t dv, lr_dtype io);
+
+int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g,
+                 const float *S0, void *o, float *S_final,
+                 int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
+                 int64_t chunk, lr_dtype io,
+                 void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Tuning and test hooks                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Overrides the number of time splits the two diagonal scans use (0 =
+ * automatic).  With more than one split, consecutive time ranges of a
+ * channel block run in different thread blocks that pass their carries by a
+ * decoupled look-back; workspace sizes follow the override.  Process-wide,
+ * not thread-safe.  Returns the previous value.
+ */
+int lr_set_split_override(int splits);
+
+/*
+ * Test hook for the bounded look-back wait: when `split` >= 1, the thread
+ * blocks of that time split never publish their carries, so their successors'
+ * waits run out (after about `timeout_ms` milliseconds), set LR_ERR_TIMEOUT
+ * and finish with a zero carry.  -1 disables.  Process-wide, not
+ * thread-safe.  Returns LR_OK.
+ */
+int lr_test_withhold_split(int split, int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRSCAN_H */

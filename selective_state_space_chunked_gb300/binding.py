@@ -1,0 +1,274 @@
+"""ctypes binding of ``liblrscan.so`` (the C ABI in ``include/lrscan.h``).
+
+Two layers, both argument marshalling only -- every step of every scan runs
+in the library's CUDA kernels:
+
+* ``lr_*`` functions with the C names and signatures (pointers as ints);
+* torch conveniences (:func:`selective_scan`, :func:`rglru_scan`,
+  :func:`hgrn2`) that check shapes and dtypes, allocate outputs and the
+  workspace with torch, pass the current CUDA stream and raise
+  :class:`LrError` on a non-zero status.  Given host tensors they copy the
+  inputs to the current CUDA device and the outputs back (the end-to-end
+  path); given device tensors they stay on the device.
+
+There is no fallback: if the library is missing this module raises at import.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+LR_F32, LR_BF16 = 0, 1
+LR_OK = 0
+LR_ERR_INVALID_ARG, LR_ERR_UNSUPPORTED, LR_ERR_MISALIGNED = -1, -2, -3
+LR_ERR_WORKSPACE, LR_ERR_CUDA, LR_ERR_TIMEOUT, LR_ERR_RANGE = -4, -5, -6, -7
+
+_IO = {torch.float32: LR_F32, torch.bfloat16: LR_BF16}
+
+# (name, restype, argtypes) of every exported C symbol
+_P, _I64, _F, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "lr_status_string": (ctypes.c_char_p, [_I]),
+    "lr_version": (_I, []),
+    "lr_check_status": (_I, [_P]),
+    "lr_set_split_override": (_I, [_I]),
+    "lr_test_withhold_split": (_I, [_I, _I]),
+    "lr_selective_scan_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I]),
+    "lr_selective_scan_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _I64, _I64, _I64, _I64, _I, _I, _P, _SZ, _P]),
+    "lr_rglru_scan_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "lr_rglru_scan_fwd": (_I, [_P, _P, _P, _P, _F, _P, _P, _P,
+                               _I64, _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_hgrn2_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I]),
+    "lr_hgrn2_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                          _I64, _I64, _I, _P, _SZ, _P]),
+}
+
+
+def _load():
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with selective_state_space_chunked_gb300."
+            "build.build() (nvcc, sm_103a). There is no CPU fallback.")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+LIB_PATH = _build.LIB_PATH
+
+
+class LrError(RuntimeError):
+    """A non-zero lrscan status."""
+
+    def __init__(self, code: int, where: str = ""):
+        self.code = int(code)
+        msg = lr_status_string(code)
+        super().__init__(f"{where}: {msg}" if where else msg)
+
+
+# ---------------------------------------------------------------- C names
+def lr_status_string(code: int) -> str:
+    return _lib.lr_status_string(int(code)).decode()
+
+
+def lr_version() -> int:
+    return int(_lib.lr_version())
+
+
+def lr_check_status(stream: int = 0) -> int:
+    return int(_lib.lr_check_status(stream or None))
+
+
+def lr_set_split_override(splits: int) -> int:
+    return int(_lib.lr_set_split_override(int(splits)))
+
+
+def lr_test_withhold_split(split: int, timeout_ms: int = 1000) -> int:
+    return int(_lib.lr_test_withhold_split(int(split), int(timeout_ms)))
+
+
+def lr_selective_scan_workspace_size(B, L, D, N, io) -> int:
+    return int(_lib.lr_selective_scan_workspace_size(B, L, D, N, io))
+
+
+def lr_selective_scan_fwd(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final,
+                          B, L, D, N, io, dt_softplus, workspace, ws_bytes,
+                          stream) -> int:
+    return int(_lib.lr_selective_scan_fwd(x, dt, z, Bm, Cm, A_log, Dskip, h0, y,
+                                          h_final, B, L, D, N, io, dt_softplus,
+                                          workspace, ws_bytes, stream))
+
+
+def lr_rglru_scan_workspace_size(B, L, D, io) -> int:
+    return int(_lib.lr_rglru_scan_workspace_size(B, L, D, io))
+
+
+def lr_rglru_scan_fwd(x, r, i, a_log, c, h0, y, h_final, B, L, D, io,
+                      workspace, ws_bytes, stream) -> int:
+    return int(_lib.lr_rglru_scan_fwd(x, r, i, a_log, c, h0, y, h_final, B, L, D,
+                                      io, workspace, ws_bytes, stream))
+
+
+def lr_hgrn2_workspace_size(B, L, H, dk, dv, io) -> int:
+    return int(_lib.lr_hgrn2_workspace_size(B, L, H, dk, dv, io))
+
+
+def lr_hgrn2_fwd(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io,
+                 workspace, ws_bytes, stream) -> int:
+    return int(_lib.lr_hgrn2_fwd(q, k, v, g, S0, o, S_final, B, L, H, dk, dv,
+                                 chunk, io, workspace, ws_bytes, stream))
+
+
+# ------------------------------------------------------------ torch helpers
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: Optional[torch.Tensor], device) -> Optional[torch.Tensor]:
+    if t is None:
+        return None
+    if t.device.type != "cuda":
+        t = t.to(device, non_blocking=True)
+    return t.contiguous()
+
+
+def _check(rc: int, where: str):
+    if rc != LR_OK:
+        raise LrError(rc, where)
+
+
+def _io_of(t: torch.Tensor) -> int:
+    if t.dtype not in _IO:
+        raise TypeError(f"unsupported I/O dtype {t.dtype}; use float32 or bfloat16")
+    return _IO[t.dtype]
+
+
+def _same(ref: torch.Tensor, *ts):
+    for t in ts:
+        if t is not None and t.dtype != ref.dtype:
+            raise TypeError("all activation tensors must share one dtype")
+
+
+def _workspace(nbytes: int, device, given: Optional[torch.Tensor]):
+    if nbytes == (1 << 64) - 1:
+        raise LrError(LR_ERR_CUDA, "workspace size query")
+    if nbytes == 0:
+        return None, 0
+    if given is not None:
+        return given, given.numel() * given.element_size()
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+def _target_device(*ts):
+    for t in ts:
+        if t is not None and t.device.type == "cuda":
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _back(out: torch.Tensor, host: bool) -> torch.Tensor:
+    if not host:
+        return out
+    h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h.copy_(out, non_blocking=True)
+    return h
+
+
+def selective_scan(x, dt, Bm, Cm, A_log, z=None, Dskip=None, h0=None,
+                   dt_softplus: bool = True, workspace=None,
+                   sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Selective SSM scan.  x, dt, z: (B, L, D); Bm, Cm: (B, L, 16), all one
+    dtype (float32 or bfloat16); A_log: (D, 16) fp32; Dskip: (D,) fp32;
+    h0: (B, D, 16) fp32.  Returns (y (B, L, D) in the I/O dtype, h_final
+    (B, D, 16) fp32).  Host inputs are copied to the GPU and results back."""
+    host = x.device.type != "cuda"
+    dev = _target_device(x)
+    x, dt, z, Bm, Cm = (_dev(t, dev) for t in (x, dt, z, Bm, Cm))
+    A_log, Dskip, h0 = (_dev(None if t is None else t.float(), dev) for t in (A_log, Dskip, h0))
+    _same(x, dt, z, Bm, Cm)
+    io = _io_of(x)
+    B, L, D = x.shape
+    N = Bm.shape[-1]
+    y = torch.empty_like(x)
+    hf = torch.empty(B, D, N, dtype=torch.float32, device=dev)
+    ws, wsb = _workspace(lr_selective_scan_workspace_size(B, L, D, N, io), dev, workspace)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(lr_selective_scan_fwd(_ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm),
+                                 _ptr(A_log), _ptr(Dskip), _ptr(h0), _ptr(y),
+                                 _ptr(hf), B, L, D, N, io, int(bool(dt_softplus)),
+                                 _ptr(ws), wsb, stream), "lr_selective_scan_fwd")
+    y, hf = _back(y, host), _back(hf, host)
+    if host and sync_host:
+        torch.cuda.current_stream(dev).synchronize()
+    return y, hf
+
+
+def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None,
+               sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
+    """RG-LRU scan.  x, r, i: (B, L, D) (r, i after their sigmoid), one dtype;
+    a_log: (D,) fp32; h0: (B, D) fp32.  Returns (y (B, L, D), h_final (B, D)
+    fp32)."""
+    host = x.device.type != "cuda"
+    dev = _target_device(x)
+    x, r, i = (_dev(t, dev) for t in (x, r, i))
+    a_log, h0 = (_dev(None if t is None else t.float(), dev) for t in (a_log, h0))
+    _same(x, r, i)
+    io = _io_of(x)
+    B, L, D = x.shape
+    y = torch.empty_like(x)
+    hf = torch.empty(B, D, dtype=torch.float32, device=dev)
+    ws, wsb = _workspace(lr_rglru_scan_workspace_size(B, L, D, io), dev, workspace)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(lr_rglru_scan_fwd(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c),
+                             _ptr(h0), _ptr(y), _ptr(hf), B, L, D, io, _ptr(ws),
+                             wsb, stream), "lr_rglru_scan_fwd")
+    y, hf = _back(y, host), _back(hf, host)
+    if host and sync_host:
+        torch.cuda.current_stream(dev).synchronize()
+    return y, hf
+
+
+def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None,
+          sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
+    """HGRN2 matrix-state recurrence.  q, k: (B, L, H*dk); v, g: (B, L, H*dv)
+    (g after its activation and lower bound), bfloat16; S0: (B, H, dv, dk)
+    fp32.  Returns (o (B, L, H*dv), S_final (B, H, dv, dk) fp32).  Raises
+    ValueError when the hidden size is not divisible by the head count."""
+    if q.shape[-1] % H or v.shape[-1] % H:
+        raise ValueError(f"hidden size {q.shape[-1]} is not divisible by {H} heads")
+    host = q.device.type != "cuda"
+    dev = _target_device(q)
+    q, k, v, g = (_dev(t, dev) for t in (q, k, v, g))
+    S0 = _dev(None if S0 is None else S0.float(), dev)
+    _same(q, k, v, g)
+    io = _io_of(q)
+    B, L, HK = q.shape
+    dk, dv = HK // H, v.shape[-1] // H
+    o = torch.empty(B, L, H * dv, dtype=q.dtype, device=dev)
+    Sf = torch.empty(B, H, dv, dk, dtype=torch.float32, device=dev)
+    ws, wsb = _workspace(lr_hgrn2_workspace_size(B, L, H, dk, dv, io), dev, workspace)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(lr_hgrn2_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0), _ptr(o),
+                        _ptr(Sf), B, L, H, dk, dv, chunk, io, _ptr(ws), wsb,
+                        stream), "lr_hgrn2_fwd")
+    o, Sf = _back(o, host), _back(Sf, host)
+    if host and sync_host:
+        torch.cuda.current_stream(dev).synchronize()
+    return o, Sf
+
+
+def check_status(stream=None) -> None:
+    """Synchronises the stream and raises on a device-side status."""
+    s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    _check(lr_check_status(s), "device status")

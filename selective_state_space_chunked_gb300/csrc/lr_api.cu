@@ -1,0 +1,209 @@
+// lr_api.cu -- the C ABI declared in include/lrscan.h: argument validation
+// (pure host logic, run before any CUDA call), dispatch to the kernels'
+// launchers, the sticky device status, and the tuning / test knobs.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "lr_internal.h"
+#include "lrscan.h"
+
+namespace lr {
+int g_split_override = 0;
+int g_withheld_split = -1;
+int g_withheld_timeout_ms = 1000;
+}  // namespace lr
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+
+bool misaligned(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+bool io_ok(lr_dtype io) { return io == LR_F32 || io == LR_BF16; }
+
+// Channel counts must keep every TMA row stride a multiple of 16 bytes.
+bool channels_ok(int64_t D, lr_dtype io) { return D % (io == LR_BF16 ? 8 : 4) == 0; }
+
+bool fits_int(int64_t v) { return v <= INT_MAX; }
+
+int check_workspace(const lr::DiagPlan &p, const void *ws, size_t ws_bytes) {
+    if (p.ws_bytes == 0) return LR_OK;
+    if (ws == nullptr || ws_bytes < p.ws_bytes) return LR_ERR_WORKSPACE;
+    if (misaligned(ws)) return LR_ERR_MISALIGNED;
+    return LR_OK;
+}
+
+// L == 0: the final state is the initial state (or zero).
+int copy_state(const float *h0, float *h_final, size_t count, cudaStream_t stream) {
+    if (h_final == nullptr || count == 0) return LR_OK;
+    const cudaError_t e =
+        h0 != nullptr
+            ? cudaMemcpyAsync(h_final, h0, count * sizeof(float), cudaMemcpyDeviceToDevice, stream)
+            : cudaMemsetAsync(h_final, 0, count * sizeof(float), stream);
+    return e == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+int validate_selective(const void *x, const void *dt, const void *z, const void *Bm,
+                       const void *Cm, const float *A_log, const float *Dskip, const float *h0,
+                       const void *y, const float *h_final, int64_t B, int64_t L, int64_t D,
+                       int64_t N, lr_dtype io) {
+    if (B < 0 || L < 0 || D < 0 || N < 0 || !io_ok(io)) return LR_ERR_INVALID_ARG;
+    // activation pointers may be NULL only when there are no activations
+    const bool acts = B > 0 && L > 0 && D > 0;
+    if ((acts && (!x || !dt || !Bm || !Cm || !y)) || (D > 0 && !A_log)) return LR_ERR_INVALID_ARG;
+    if (N != 16 || !channels_ok(D, io)) return LR_ERR_UNSUPPORTED;
+    if (!fits_int(B) || !fits_int(L) || !fits_int(D)) return LR_ERR_UNSUPPORTED;
+    const void *ptrs[] = {x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final};
+    for (const void *p : ptrs)
+        if (misaligned(p)) return LR_ERR_MISALIGNED;
+    return LR_OK;
+}
+
+int validate_rglru(const void *x, const void *r, const void *i, const float *a_log, float c,
+                   const float *h0, const void *y, const float *h_final, int64_t B, int64_t L,
+                   int64_t D, lr_dtype io) {
+    if (B < 0 || L < 0 || D < 0 || !io_ok(io) || !std::isfinite(c)) return LR_ERR_INVALID_ARG;
+    const bool acts = B > 0 && L > 0 && D > 0;
+    if ((acts && (!x || !r || !i || !y)) || (D > 0 && !a_log)) return LR_ERR_INVALID_ARG;
+    if (!channels_ok(D, io)) return LR_ERR_UNSUPPORTED;
+    if (!fits_int(B) || !fits_int(L) || !fits_int(D)) return LR_ERR_UNSUPPORTED;
+    const void *ptrs[] = {x, r, i, a_log, h0, y, h_final};
+    for (const void *p : ptrs)
+        if (misaligned(p)) return LR_ERR_MISALIGNED;
+    return LR_OK;
+}
+
+int validate_hgrn2(const void *q, const void *k, const void *v, const void *g, const float *S0,
+                   const void *o, const float *S_final, int64_t B, int64_t L, int64_t H,
+                   int64_t dk, int64_t dv, int64_t chunk, lr_dtype io) {
+    if (B < 0 || L < 0 || H <= 0 || dk <= 0 || dv <= 0 || chunk <= 0 || !io_ok(io))
+        return LR_ERR_INVALID_ARG;
+    if (B > 0 && L > 0 && (!q || !k || !v || !g || !o)) return LR_ERR_INVALID_ARG;
+    if (dk != 128 || dv != 128 || chunk != 64 || io != LR_BF16) return LR_ERR_UNSUPPORTED;
+    if (!fits_int(B) || !fits_int(L) || !fits_int(H) || !fits_int(B * H)) return LR_ERR_UNSUPPORTED;
+    const void *ptrs[] = {q, k, v, g, S0, o, S_final};
+    for (const void *p : ptrs)
+        if (misaligned(p)) return LR_ERR_MISALIGNED;
+    return LR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lr_status_string(int code) {
+    switch (code) {
+        case LR_OK: return "LR_OK";
+        case LR_ERR_INVALID_ARG: return "LR_ERR_INVALID_ARG: invalid argument";
+        case LR_ERR_UNSUPPORTED: return "LR_ERR_UNSUPPORTED: unsupported shape or dtype";
+        case LR_ERR_MISALIGNED: return "LR_ERR_MISALIGNED: tensor base not 16-byte aligned";
+        case LR_ERR_WORKSPACE: return "LR_ERR_WORKSPACE: workspace missing or too small";
+        case LR_ERR_CUDA: return "LR_ERR_CUDA: a CUDA call failed";
+        case LR_ERR_TIMEOUT: return "LR_ERR_TIMEOUT: a bounded device-side wait ran out";
+        case LR_ERR_RANGE: return "LR_ERR_RANGE: HGRN2 chunk log-gate spread too wide";
+        default: return "unknown lrscan status";
+    }
+}
+
+int lr_version(void) { return kVersion; }
+
+int lr_check_status(lr_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LR_ERR_CUDA;
+    int s1 = 0, s2 = 0;
+    if (lr::diag_status_read_and_clear(&s1) != LR_OK) return LR_ERR_CUDA;
+    if (lr::hgrn2_status_read_and_clear(&s2) != LR_OK) return LR_ERR_CUDA;
+    return s1 != 0 ? s1 : s2;
+}
+
+int lr_set_split_override(int splits) {
+    const int prev = lr::g_split_override;
+    lr::g_split_override = splits > 0 ? splits : 0;
+    return prev;
+}
+
+int lr_test_withhold_split(int split, int timeout_ms) {
+    lr::g_withheld_split = split >= 1 ? split : -1;
+    lr::g_withheld_timeout_ms = timeout_ms > 0 ? timeout_ms : 1000;
+    return LR_OK;
+}
+
+// ---------------------------------------------------------------- selective
+size_t lr_selective_scan_workspace_size(int64_t B, int64_t L, int64_t D, int64_t N, lr_dtype io) {
+    if (B <= 0 || L <= 0 || D <= 0 || N != 16 || !io_ok(io)) return 0;
+    lr::DiagPlan p;
+    if (lr::selective_plan(B, L, D, io, &p) != LR_OK) return SIZE_MAX;
+    return p.ws_bytes;
+}
+
+int lr_selective_scan_fwd(const void *x, const void *dt, const void *z, const void *Bm,
+                          const void *Cm, const float *A_log, const float *Dskip, const float *h0,
+                          void *y, float *h_final, int64_t B, int64_t L, int64_t D, int64_t N,
+                          lr_dtype io, int dt_softplus, void *workspace, size_t ws_bytes,
+                          lr_stream_t stream) {
+    int rc = validate_selective(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, N, io);
+    if (rc != LR_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return LR_OK;
+    if (L == 0) return copy_state(h0, h_final, size_t(B) * D * N, st);
+    lr::DiagPlan p;
+    if ((rc = lr::selective_plan(B, L, D, io, &p)) != LR_OK) return rc;
+    if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
+    return lr::selective_launch(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, io,
+                                dt_softplus, p, workspace, st);
+}
+
+// ---------------------------------------------------------------- RG-LRU
+size_t lr_rglru_scan_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io) {
+    if (B <= 0 || L <= 0 || D <= 0 || !io_ok(io)) return 0;
+    lr::DiagPlan p;
+    if (lr::rglru_plan(B, L, D, io, &p) != LR_OK) return SIZE_MAX;
+    return p.ws_bytes;
+}
+
+int lr_rglru_scan_fwd(const void *x, const void *r, const void *i, const float *a_log, float c,
+                      const float *h0, void *y, float *h_final, int64_t B, int64_t L, int64_t D,
+                      lr_dtype io, void *workspace, size_t ws_bytes, lr_stream_t stream) {
+    int rc = validate_rglru(x, r, i, a_log, c, h0, y, h_final, B, L, D, io);
+    if (rc != LR_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return LR_OK;
+    if (L == 0) return copy_state(h0, h_final, size_t(B) * D, st);
+    lr::DiagPlan p;
+    if ((rc = lr::rglru_plan(B, L, D, io, &p)) != LR_OK) return rc;
+    if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
+    return lr::rglru_launch(x, r, i, a_log, c, h0, y, h_final, B, L, D, io, p, workspace, st);
+}
+
+// ---------------------------------------------------------------- HGRN2
+size_t lr_hgrn2_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
+                               lr_dtype io) {
+    (void)dk;
+    (void)dv;
+    (void)io;
+    size_t bytes = 0;
+    if (B <= 0 || L <= 0 || H <= 0) return 0;
+    if (lr::hgrn2_workspace(B, L, H, &bytes) != LR_OK) return SIZE_MAX;
+    return bytes;
+}
+
+int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g, const float *S0,
+                 void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
+                 int64_t chunk, lr_dtype io, void *workspace, size_t ws_bytes,
+                 lr_stream_t stream) {
+    int rc = validate_hgrn2(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io);
+    if (rc != LR_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (B == 0) return LR_OK;
+    if (L == 0) return copy_state(S0, S_final, size_t(B) * H * dk * dv, st);
+    size_t need = 0;
+    if ((rc = lr::hgrn2_workspace(B, L, H, &need)) != LR_OK) return rc;
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return LR_ERR_WORKSPACE;
+    if (misaligned(workspace)) return LR_ERR_MISALIGNED;
+    return lr::hgrn2_launch(q, k, v, g, S0, o, S_final, B, L, H, workspace, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,996 @@
+// lr_diag_scan.cu -- the two diagonal-state scans on sm_103a:
+//
+//   * RG-LRU   (lrnnx rglru module source, RGLRU.step fallback update):
+//       a_t = exp(c r_t a_log),  h = a_t h + sqrt(1 - a_t^2) (i_t x_t),  y_t = h
+//   * selective SSM (cortexnet 3.2.1, cortexnet/ssm.py, MultiScaleSSM):
+//       delta = softplus(dt), h[n] = exp(delta A[n]) h[n] + delta B_t[n] x,
+//       y_t = (C_t . h + D x) silu(z)
+//
+// Design (both kernels):
+//   * A thread block owns a block of DC consecutive channels of one batch row
+//     and streams a range of time tiles (T steps x DC channels) through a
+//     multi-stage shared-memory ring filled by TMA (cp.async.bulk.tensor,
+//     3-D maps over (D, L, B); out-of-range rows and channels arrive as
+//     zeros).  Warps are specialised: a producer warp keeps the ring full
+//     (and widens shared per-step operands once per tile), compute warps
+//     run the recurrence of their channels (one thread per channel, or a
+//     lane pair per channel for the 16-state selective scan) with the state
+//     in registers, in batches of 8 steps whose loads and coefficients are
+//     independent, and store outputs straight from registers.  Stages pass
+//     between the roles through full / empty mbarriers, not block barriers.
+//   * When batch x channel blocks fill the GPU (S == 1) a block streams the
+//     whole sequence once, carrying the state across tiles in registers.
+//   * Otherwise the sequence is cut into S time splits that run in parallel.
+//     Each split first scans its range from a zero state to get its
+//     aggregate (product of decays, state), publishes it, and
+//     takes its carry-in from a decoupled look-back over the preceding
+//     splits' descriptors (Merrill & Garland, "Single-pass Parallel Prefix
+//     Scan with Decoupled Look-back", 2016).  Split order comes from an
+//     atomic ticket, so every split a block waits for is already running.
+//     It then re-streams its range (an L2 hit for the small problems this
+//     mode serves) and writes the outputs.  Every wait is bounded in time.
+//   * A split descriptor is (product of decays, h) per channel for RG-LRU and
+//     (sum of delta, h[16]) for the selective scan, whose 16 decay products
+//     over a range are exp(A[n] sum delta) and need not be stored.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "lr_device.cuh"
+#include "lr_internal.h"
+
+namespace lr {
+
+__device__ int g_diag_status = 0;
+
+__device__ __forceinline__ void report_status(int code) { atomicCAS(&g_diag_status, 0, code); }
+
+// Flag values of a split descriptor.
+constexpr uint32_t kFlagNone = 0, kFlagAggregate = 1, kFlagInclusive = 2;
+
+struct LookbackWs {
+    uint32_t *flags;   // [n_cb * S]
+    uint32_t *ticket;  // [1]
+    float *agg;        // [n_cb * S][kAgg][DC]
+    float *incl;       // [n_cb * S][kIncl][DC]
+};
+
+// Polls a split flag (thread 0 only) until it is non-zero or the limit runs
+// out; returns the flag value (kFlagNone on timeout).
+__device__ __forceinline__ uint32_t poll_flag(const uint32_t *flag, uint64_t limit_ns) {
+    uint32_t v = ld_acquire_gpu(flag);
+    if (v != kFlagNone) return v;
+    const uint64_t t0 = globaltimer_ns();
+    while ((v = ld_acquire_gpu(flag)) == kFlagNone) {
+        if (globaltimer_ns() - t0 > limit_ns) return kFlagNone;
+        __nanosleep(100);
+    }
+    return v;
+}
+
+// ----------------------------------------------------------------------------
+// Accurate helpers (fp32 I/O path)
+// ----------------------------------------------------------------------------
+
+// exp(x) - 1 without cancellation: Taylor series (coefficients 1/k!) for
+// |x| < 0.3, where nine terms leave a truncation error below 2e-12 relative;
+// expf(x) - 1 elsewhere, where |exp(x) - 1| > 0.25 keeps the subtraction
+// exact to a few ulp.
+__device__ __forceinline__ float expm1_accurate(float x) {
+    if (fabsf(x) < 0.3f) {
+        float p = 1.0f / 362880.0f;
+        p = fmaf(p, x, 1.0f / 40320.0f);
+        p = fmaf(p, x, 1.0f / 5040.0f);
+        p = fmaf(p, x, 1.0f / 720.0f);
+        p = fmaf(p, x, 1.0f / 120.0f);
+        p = fmaf(p, x, 1.0f / 24.0f);
+        p = fmaf(p, x, 1.0f / 6.0f);
+        p = fmaf(p, x, 0.5f);
+        p = fmaf(p, x, 1.0f);
+        return p * x;
+    }
+    return expf(x) - 1.0f;
+}
+
+// torch softplus (beta 1, threshold 20).
+template <bool ACC>
+__device__ __forceinline__ float softplus_t(float x) {
+    if (ACC) return x > 20.0f ? x : log1pf(expf(x));
+    const float e = ex2_approx(x * kLog2e);
+    // log(1 + e): for small e the series e (1 - e/2) keeps e's digits that
+    // 1 + e would round away (series error below e^3 / 3).
+    const float l = e < 1e-3f ? e * fmaf(-0.5f, e, 1.0f) : lg2_approx(1.0f + e) * kLn2;
+    return x > 20.0f ? x : l;
+}
+
+__device__ __forceinline__ float silu_f(float z) {
+    return z * rcp_approx(1.0f + ex2_approx(-z * kLog2e));
+}
+
+template <bool ACC>
+__device__ __forceinline__ float pow2_t(float e) {
+    return ACC ? exp2f(e) : ex2_approx(e);
+}
+
+// ============================================================================
+// Shared tile helpers
+// ============================================================================
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Two consecutive bf16 / fp32 values as a float2.
+__device__ __forceinline__ float2 ld2(const float *p) { return *reinterpret_cast<const float2 *>(p); }
+__device__ __forceinline__ float2 ld2(const __nv_bfloat16 *p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+}
+
+// Per-block abort word: once any wait of the block has run out, later waits
+// are skipped so that every warp still walks the same barrier sequence and
+// the block finishes.
+__device__ __noinline__ bool block_wait_slow(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                             volatile int *flag) {
+    if (*flag != 0) return false;
+    if (mbar_wait_bounded(bar, parity, limit_ns)) return true;
+    *flag = 1;
+    report_status(LR_ERR_TIMEOUT);
+    return false;
+}
+
+struct BlockAbort {
+    volatile int *flag;
+    // Fast path: one try_wait when the phase has already completed.
+    __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) const {
+        if (mbar_try_wait(bar, parity)) return true;
+        return block_wait_slow(bar, parity, limit_ns, flag);
+    }
+};
+
+// ============================================================================
+// RG-LRU
+// ============================================================================
+// Warp roles in a block of DC channels:
+//   compute warps (one channel per thread): wait for a TMA-staged tile, then
+//     run the recurrence through it in batches of 8 steps (loads, a_t, b_t of
+//     the batch are independent; only the h chain is sequential) and store
+//     y straight from registers; then release the stage (one arrive per warp).
+//   producer warp: lane 0 keeps STAGES tiles of x, r, i in flight by TMA,
+//     re-arming a stage as soon as every compute warp released it.
+template <typename IO>
+struct RgCfg {
+    static constexpr int DC = 64;                        // channels per block
+    static constexpr int T = 32;                         // time steps per tile
+    static constexpr int CWARPS = DC / 32;
+    static constexpr int THREADS = 32 * (CWARPS + 1);    // + producer warp
+    static constexpr int STAGES = sizeof(IO) == 2 ? 6 : 4;
+    static constexpr int BATCH = 8;
+    static constexpr int TILE = T * DC;
+    static constexpr uint32_t STAGE_BYTES = 3u * TILE * sizeof(IO);
+    static constexpr size_t OFF_BAR = size_t(STAGES) * STAGE_BYTES;   // full[], empty[]
+    static constexpr size_t SMEM = OFF_BAR + 2 * STAGES * 8 + 16;
+    static constexpr int kAgg = 2, kIncl = 1;  // descriptor floats per channel
+};
+
+// a_t and b_t = sqrt(1 - a_t^2) u of one (t, channel); cl = c a_log,
+// cl2 = cl log2(e).
+template <bool ACC>
+__device__ __forceinline__ void rglru_ab(float r, float u, float cl, float cl2, float &a,
+                                         float &bb) {
+    if (ACC) {
+        const float em1 = expm1_accurate(cl * r);   // a_t - 1
+        a = 1.0f + em1;
+        bb = sqrtf(-em1 * (2.0f + em1)) * u;        // 1 - a^2 = -em1 (2 + em1)
+    } else {
+        a = ex2_approx(cl2 * r);
+        bb = sqrt_approx(fmaf(-a, a, 1.0f)) * u;
+    }
+}
+
+// Tile modes: the aggregate pass, an output tile whose rows and channels are
+// all in range (no per-step predicate, so a batch is one basic block the
+// scheduler can interleave), and a ragged output tile.
+enum TileMode { kAggregate = 0, kFull = 1, kRagged = 2 };
+
+// One T-step tile of one channel's recurrence.
+template <typename IO, bool ACC, int MODE>
+__device__ __forceinline__ void rglru_tile(const IO *xs, const IO *rs, const IO *is, float cl,
+                                           float cl2, float &h, float &P, IO *yp, int D, int rows) {
+    using C = RgCfg<IO>;
+#pragma unroll
+    for (int j0 = 0; j0 < C::T; j0 += C::BATCH) {
+        float a[C::BATCH], bb[C::BATCH];
+#pragma unroll
+        for (int u = 0; u < C::BATCH; ++u) {
+            const int o = (j0 + u) * C::DC;
+            rglru_ab<ACC>(Io<IO>::to_f(rs[o]), Io<IO>::to_f(is[o]) * Io<IO>::to_f(xs[o]), cl, cl2,
+                          a[u], bb[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < C::BATCH; ++u) {
+            h = fmaf(a[u], h, bb[u]);
+            if (MODE == kAggregate) P *= a[u];
+            if (MODE == kFull) __stcs(yp + size_t(j0 + u) * D, Io<IO>::from_f(h));
+            if (MODE == kRagged && j0 + u < rows) __stcs(yp + size_t(j0 + u) * D, Io<IO>::from_f(h));
+        }
+    }
+}
+
+template <typename IO, bool ACC>
+__global__ void __launch_bounds__(RgCfg<IO>::THREADS)
+    rglru_scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_r,
+                      const __grid_constant__ CUtensorMap tm_i, const float *__restrict__ a_log,
+                      float c, const float *__restrict__ h0, IO *__restrict__ y,
+                      float *__restrict__ h_final, int L, int D, int n_db, int S, int tps,
+                      int n_tiles, LookbackWs ws, int withheld, uint64_t timeout_ns) {
+    using C = RgCfg<IO>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    IO *tiles = reinterpret_cast<IO *>(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *empty = full + C::STAGES;
+    int *bcast = reinterpret_cast<int *>(empty + C::STAGES);
+    int *abort_word = bcast + 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const BlockAbort ab{abort_word};
+
+    if (tid == 0) {
+        for (int st = 0; st < C::STAGES; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], C::CWARPS);
+        }
+        *abort_word = 0;
+        fence_mbar_init();
+        if (S > 1) *bcast = static_cast<int>(atomicAdd(ws.ticket, 1u));
+    }
+    __syncthreads();
+    const int tk = S > 1 ? *bcast : static_cast<int>(blockIdx.x);
+    const int cb = tk / S, s = tk - (tk / S) * S;
+    const int b = cb / n_db;
+    const int d0 = (cb - b * n_db) * C::DC;
+    const int k0 = s * tps;
+    const int ntl = min(k0 + tps, n_tiles) - k0;
+    const int V = S > 1 ? 2 * ntl : ntl;  // virtual tiles: aggregate pass, then output pass
+
+    if (warp == C::CWARPS) {  // ---------------------------------- producer warp
+        if (lane == 0) {
+            prefetch_tensormap(&tm_x);
+            prefetch_tensormap(&tm_r);
+            prefetch_tensormap(&tm_i);
+            for (int v = 0; v < V; ++v) {
+                const int st = v % C::STAGES;
+                if (v >= C::STAGES && !ab.wait(&empty[st], ((v / C::STAGES) - 1) & 1, timeout_ns))
+                    break;
+                const int t0 = (k0 + v % ntl) * C::T;
+                IO *base = tiles + size_t(st) * 3 * C::TILE;
+                mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+                tma_load_3d(base, &tm_x, &full[st], d0, t0, b);
+                tma_load_3d(base + C::TILE, &tm_r, &full[st], d0, t0, b);
+                tma_load_3d(base + 2 * C::TILE, &tm_i, &full[st], d0, t0, b);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ compute warps
+    const int ch = tid;  // channel within the block
+    const int d = d0 + ch;
+    const bool vd = d < D;
+    const float cl = vd ? c * a_log[d] : 0.0f;
+    const float cl2 = cl * kLog2e;
+    const float h0v = (vd && h0 != nullptr) ? h0[size_t(b) * D + d] : 0.0f;
+    float h = S > 1 ? 0.0f : h0v;  // the aggregate pass starts from zero
+    float P = 1.0f;                // product of decays over the aggregate pass
+
+    for (int v = 0; v < V; ++v) {
+        const int st = v % C::STAGES;
+        const bool agg_pass = S > 1 && v < ntl;
+        const int t0 = (k0 + v % ntl) * C::T;
+        ab.wait(&full[st], (v / C::STAGES) & 1, timeout_ns);
+        const IO *xs = tiles + size_t(st) * 3 * C::TILE + ch;
+        const IO *rs = xs + C::TILE;
+        const IO *is = rs + C::TILE;
+        IO *yp = y + (size_t(b) * L + t0) * D + d;
+        // warp-uniform choice: the whole warp's channels and rows in range?
+        const bool full_tile = t0 + C::T <= L && d0 + 32 * (warp + 1) <= D;
+        if (agg_pass)
+            rglru_tile<IO, ACC, kAggregate>(xs, rs, is, cl, cl2, h, P, yp, D, 0);
+        else if (full_tile)
+            rglru_tile<IO, ACC, kFull>(xs, rs, is, cl, cl2, h, P, yp, D, C::T);
+        else
+            rglru_tile<IO, ACC, kRagged>(xs, rs, is, cl, cl2, h, P, yp, D, vd ? min(C::T, L - t0) : 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+
+        if (agg_pass && v == ntl - 1) {
+            // ---- publish this split's aggregate, look back, publish inclusive
+            constexpr int NC = 32 * C::CWARPS;
+            const size_t slot = size_t(cb) * S + s;
+            float carry = h0v;
+            if (s > 0) {
+                ws.agg[(slot * C::kAgg + 0) * C::DC + ch] = P;
+                ws.agg[(slot * C::kAgg + 1) * C::DC + ch] = h;
+                __threadfence();
+                named_bar_sync(1, NC);
+                if (tid == 0 && s != withheld) st_release_gpu(&ws.flags[slot], kFlagAggregate);
+                float acc_p = 1.0f, acc_h = 0.0f;  // composition of splits sp+1 .. s-1
+                carry = 0.0f;
+                for (int sp = s - 1; sp >= 0; --sp) {
+                    const size_t sl = size_t(cb) * S + sp;
+                    if (tid == 0) *bcast = static_cast<int>(poll_flag(&ws.flags[sl], timeout_ns));
+                    named_bar_sync(1, NC);
+                    const int fv = *bcast;
+                    named_bar_sync(1, NC);
+                    if (fv == static_cast<int>(kFlagInclusive)) {
+                        carry = fmaf(acc_p, __ldcg(&ws.incl[sl * C::DC + ch]), acc_h);
+                        break;
+                    }
+                    if (fv == static_cast<int>(kFlagAggregate)) {
+                        const float px = __ldcg(&ws.agg[(sl * C::kAgg + 0) * C::DC + ch]);
+                        const float hx = __ldcg(&ws.agg[(sl * C::kAgg + 1) * C::DC + ch]);
+                        acc_h = fmaf(acc_p, hx, acc_h);
+                        acc_p *= px;
+                        continue;
+                    }
+                    if (tid == 0) report_status(LR_ERR_TIMEOUT);
+                    carry = acc_h;
+                    break;
+                }
+            }
+            ws.incl[slot * C::DC + ch] = fmaf(P, carry, h);
+            __threadfence();
+            named_bar_sync(1, NC);
+            if (tid == 0 && s != withheld) st_release_gpu(&ws.flags[slot], kFlagInclusive);
+            h = carry;  // the output pass restarts the range from its carry-in
+        }
+    }
+    if (h_final != nullptr && vd && s == S - 1) h_final[size_t(b) * D + d] = h;
+}
+
+// ============================================================================
+// Selective SSM
+// ============================================================================
+// Warp roles in a block of DC channels:
+//   compute warps: a lane pair per channel, 8 states per lane.  In batches of
+//     8 steps each lane computes delta = softplus(dt) and u = delta x for 4
+//     of the steps and swaps them with its partner; both lanes advance their
+//     8 states through the 8 steps (h[n] = exp(delta A[n]) h[n] + u B_t[n],
+//     partial C_t . h); the pair adds its halves with 4 shuffles; each lane
+//     finishes y = (C.h + D x) silu(z) for its 4 steps and stores it.
+//   producer warp: keeps STAGES tiles of x, dt, z, B_t, C_t in flight by TMA
+//     and widens each tile's B_t, C_t rows (shared by all channels) to fp32
+//     once, so the compute lanes read them with broadcast 16-byte loads.
+template <typename IO, int DC_>
+struct SelCfg {
+    static constexpr int DC = DC_;                       // channels per block
+    static constexpr int CWARPS = DC / 16;               // 16 channels per compute warp
+    static constexpr int THREADS = 32 * (CWARPS + 1);    // + producer warp
+    static constexpr int N = 16, NH = 8;
+    static constexpr int T = 32;
+    static constexpr int STAGES = 4;
+    static constexpr int BATCH = 8;
+    static constexpr int TILE = T * DC;                  // x / dt / z tile elements
+    static constexpr int TILE_N = T * N;                 // B / C tile elements
+    static constexpr int STAGE_ELEMS = 3 * TILE + 2 * TILE_N;
+    static constexpr size_t STAGE_IO_BYTES = size_t(STAGE_ELEMS) * sizeof(IO);
+    static constexpr size_t OFF_BC = size_t(STAGES) * STAGE_IO_BYTES;     // float [STAGES][T][2N]
+    static constexpr size_t OFF_BAR = OFF_BC + size_t(STAGES) * T * 2 * N * 4;
+    static constexpr size_t SMEM = OFF_BAR + 3 * STAGES * 8 + 16;
+    static constexpr int kAgg = 1 + N, kIncl = N;
+    static_assert(T % BATCH == 0 && DC % 16 == 0, "tile shape");
+};
+
+// Advances 8 states by one step: h = exp(delta A) h + u B, and returns
+// sum_n C[n] h[n] over these states (when READOUT).
+template <bool READOUT>
+__device__ __forceinline__ float sel_step8(float2 (&h)[4], const float2 (&A2)[4], float dl, float u,
+                                           const float *Bp, const float *Cp) {
+    const float2 dd = make_float2(dl, dl);
+    const float2 uu = make_float2(u, u);
+    const float4 b0 = *reinterpret_cast<const float4 *>(Bp);
+    const float4 b1 = *reinterpret_cast<const float4 *>(Bp + 4);
+    const float2 Bv[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                          make_float2(b1.z, b1.w)};
+    float2 Cv[4];
+    if (READOUT) {
+        const float4 c0 = *reinterpret_cast<const float4 *>(Cp);
+        const float4 c1 = *reinterpret_cast<const float4 *>(Cp + 4);
+        Cv[0] = make_float2(c0.x, c0.y);
+        Cv[1] = make_float2(c0.z, c0.w);
+        Cv[2] = make_float2(c1.x, c1.y);
+        Cv[3] = make_float2(c1.z, c1.w);
+    }
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 arg = __fmul2_rn(dd, A2[q]);
+        const float2 a = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+        h[q] = __ffma2_rn(a, h[q], __fmul2_rn(uu, Bv[q]));
+        if (READOUT) acc = __ffma2_rn(Cv[q], h[q], acc);
+    }
+    return acc.x + acc.y;
+}
+
+// One T-step tile of one lane's 8 states.  `rows` = steps of the tile inside
+// the sequence (and 0 for a channel past D in the ragged mode).  MODE is
+// warp-uniform, so the lane-pair shuffles always run converged.
+template <typename IO, int DC, bool ACC, bool HAS_Z, bool SOFTPLUS, int MODE>
+__device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *zs, const float *bc,
+                                         const float2 (&A2)[4], float2 (&h)[4], float &dsum,
+                                         float dsk, IO *yp, int D, int rows, int half) {
+    using C = SelCfg<IO, DC>;
+    const unsigned FULL = 0xffffffffu;
+#pragma unroll 1
+    for (int j0 = 0; j0 < C::T; j0 += C::BATCH) {
+        // this lane owns steps j0 + half + 2m, m = 0..3
+        float xv[4], dl[4], u[4], dlo[4], uo[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int j = j0 + half + 2 * m;
+            xv[m] = Io<IO>::to_f(xs[j * DC]);
+            const float dtv = Io<IO>::to_f(dts[j * DC]);
+            dl[m] = SOFTPLUS ? softplus_t<ACC>(dtv) : dtv;
+            if (MODE != kFull) dl[m] = j < rows ? dl[m] : 0.0f;  // rows past L: identity steps
+            u[m] = dl[m] * xv[m];
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            dlo[m] = __shfl_xor_sync(FULL, dl[m], 1);
+            uo[m] = __shfl_xor_sync(FULL, u[m], 1);
+        }
+        float yq[C::BATCH];
+#pragma unroll
+        for (int q = 0; q < C::BATCH; ++q) {
+            const bool own = (q & 1) == half;
+            const float dq = own ? dl[q >> 1] : dlo[q >> 1];
+            const float uq = own ? u[q >> 1] : uo[q >> 1];
+            const float *row = bc + (j0 + q) * 2 * C::N;
+            if (MODE == kAggregate) {
+                sel_step8<false>(h, A2, dq, uq, row, row + C::N);
+                dsum += dq;
+            } else {
+                yq[q] = sel_step8<true>(h, A2, dq, uq, row, row + C::N);
+            }
+        }
+        if (MODE != kAggregate) {
+            // lane pair reduction: this lane keeps its own steps
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float mine = half ? yq[2 * m + 1] : yq[2 * m];
+                const float other = __shfl_xor_sync(FULL, half ? yq[2 * m] : yq[2 * m + 1], 1);
+                const int j = j0 + half + 2 * m;
+                float o = fmaf(dsk, xv[m], mine + other);
+                if (HAS_Z) o *= silu_f(Io<IO>::to_f(zs[j * DC]));
+                if (MODE == kFull || j < rows) __stcs(yp + size_t(j) * D, Io<IO>::from_f(o));
+            }
+        }
+    }
+}
+
+template <typename IO, int DC, bool ACC, bool HAS_Z, bool SOFTPLUS>
+__global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
+    selective_scan_kernel(const __grid_constant__ CUtensorMap tm_x,
+                          const __grid_constant__ CUtensorMap tm_dt,
+                          const __grid_constant__ CUtensorMap tm_z,
+                          const __grid_constant__ CUtensorMap tm_B,
+                          const __grid_constant__ CUtensorMap tm_C, const float *__restrict__ A_log,
+                          const float *__restrict__ Dskip, const float *__restrict__ h0,
+                          IO *__restrict__ y, float *__restrict__ h_final, int L, int D, int n_db,
+                          int S, int tps, int n_tiles, LookbackWs ws, int withheld,
+                          uint64_t timeout_ns) {
+    using C = SelCfg<IO, DC>;
+    constexpr bool has_z = HAS_Z;
+    extern __shared__ __align__(128) unsigned char smem[];
+    IO *tiles = reinterpret_cast<IO *>(smem);
+    float *BCf = reinterpret_cast<float *>(smem + C::OFF_BC);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *ready = full + C::STAGES;   // B/C widened: producer -> compute
+    uint64_t *empty = ready + C::STAGES;  // stage released: compute -> producer
+    int *bcast = reinterpret_cast<int *>(empty + C::STAGES);
+    int *abort_word = bcast + 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const BlockAbort abt{abort_word};
+    const unsigned FULL = 0xffffffffu;
+
+    if (tid == 0) {
+        for (int st = 0; st < C::STAGES; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&ready[st], 1);
+            mbar_init(&empty[st], C::CWARPS);
+        }
+        *abort_word = 0;
+        fence_mbar_init();
+        if (S > 1) *bcast = static_cast<int>(atomicAdd(ws.ticket, 1u));
+    }
+    __syncthreads();
+    const int tk = S > 1 ? *bcast : static_cast<int>(blockIdx.x);
+    const int cb = tk / S, s = tk - (tk / S) * S;
+    const int b = cb / n_db;
+    const int d0 = (cb - b * n_db) * DC;
+    const int k0 = s * tps;
+    const int ntl = min(k0 + tps, n_tiles) - k0;
+    const int V = S > 1 ? 2 * ntl : ntl;
+    const uint32_t stage_bytes =
+        uint32_t((has_z ? 3 : 2) * C::TILE + 2 * C::TILE_N) * uint32_t(sizeof(IO));
+
+    if (warp == C::CWARPS) {  // ---------------------------------- producer warp
+        auto issue = [&](int v) {  // lane 0 only
+            const int st = v % C::STAGES;
+            const int t0 = (k0 + v % ntl) * C::T;
+            IO *base = tiles + size_t(st) * C::STAGE_ELEMS;
+            mbar_arrive_expect_tx(&full[st], stage_bytes);
+            tma_load_3d(base, &tm_x, &full[st], d0, t0, b);
+            tma_load_3d(base + C::TILE, &tm_dt, &full[st], d0, t0, b);
+            if (has_z) tma_load_3d(base + 2 * C::TILE, &tm_z, &full[st], d0, t0, b);
+            tma_load_3d(base + 3 * C::TILE, &tm_B, &full[st], 0, t0, b);
+            tma_load_3d(base + 3 * C::TILE + C::TILE_N, &tm_C, &full[st], 0, t0, b);
+        };
+        if (lane == 0) {
+            prefetch_tensormap(&tm_x);
+            prefetch_tensormap(&tm_dt);
+            if (has_z) prefetch_tensormap(&tm_z);
+            prefetch_tensormap(&tm_B);
+            prefetch_tensormap(&tm_C);
+            for (int v = 0; v < min(C::STAGES, V); ++v) issue(v);
+        }
+        for (int v = 0; v < V; ++v) {
+            const int st = v % C::STAGES;
+            // widen tile v's B_t, C_t rows into BCf[st] = [T][B(16) | C(16)]
+            bool ok = true;
+            if (lane == 0) ok = abt.wait(&full[st], (v / C::STAGES) & 1, timeout_ns);
+            ok = __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+            if (ok) {
+                const IO *Bs = tiles + size_t(st) * C::STAGE_ELEMS + 3 * C::TILE;
+                float *dst = BCf + size_t(st) * C::T * 2 * C::N;
+#pragma unroll
+                for (int k = 0; k < C::TILE_N / 32; ++k) {   // pairs over B then C
+                    const int p = lane + 32 * k;
+                    const int which = p / (C::TILE_N / 2);
+                    const int e = 2 * (p - which * (C::TILE_N / 2));
+                    const float2 v2 = ld2(Bs + which * C::TILE_N + e);
+                    *reinterpret_cast<float2 *>(dst + (e / C::N) * 2 * C::N + which * C::N +
+                                                e % C::N) = v2;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ready[st]);
+                // re-arm the stage of tile v - 1 once the compute warps released it
+                const int nv = v - 1 + C::STAGES;
+                if (v >= 1 && nv < V) {
+                    const int ps = (v - 1) % C::STAGES;
+                    if (abt.wait(&empty[ps], ((v - 1) / C::STAGES) & 1, timeout_ns)) issue(nv);
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ compute warps
+    const int ch = tid >> 1;    // channel within the block
+    const int half = tid & 1;   // states [8 half, 8 half + 8)
+    const int d = d0 + ch;
+    const bool vd = d < D;
+    float2 A2[4], h[4];         // A2 = A log2(e) = -exp(A_log) log2(e)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int n = half * C::NH + 2 * q;
+        A2[q] = vd ? make_float2(-expf(A_log[size_t(d) * C::N + n]) * kLog2e,
+                                 -expf(A_log[size_t(d) * C::N + n + 1]) * kLog2e)
+                   : make_float2(0.0f, 0.0f);
+        h[q] = (vd && h0 != nullptr && S == 1)
+                   ? make_float2(h0[(size_t(b) * D + d) * C::N + n],
+                                 h0[(size_t(b) * D + d) * C::N + n + 1])
+                   : make_float2(0.0f, 0.0f);
+    }
+    const float dsk = (vd && Dskip != nullptr) ? Dskip[d] : 0.0f;
+    float dsum = 0.0f;  // sum of delta over the aggregate pass
+
+    for (int v = 0; v < V; ++v) {
+        const int st = v % C::STAGES;
+        const bool agg_pass = S > 1 && v < ntl;
+        const int t0 = (k0 + v % ntl) * C::T;
+        abt.wait(&ready[st], (v / C::STAGES) & 1, timeout_ns);
+        const IO *base = tiles + size_t(st) * C::STAGE_ELEMS;
+        const IO *xs = base + ch;
+        const IO *dts = base + C::TILE + ch;
+        const IO *zs = base + 2 * C::TILE + ch;
+        const float *bc = BCf + size_t(st) * C::T * 2 * C::N + half * C::NH;
+        IO *yp = y + (size_t(b) * L + t0) * D + d;
+        (void)FULL;
+        const bool full_tile = t0 + C::T <= L && d0 + 16 * (warp + 1) <= D;
+        if (agg_pass)
+            sel_tile<IO, DC, ACC, HAS_Z, SOFTPLUS, kAggregate>(xs, dts, zs, bc, A2, h, dsum, dsk, yp,
+                                                                D, L - t0, half);
+        else if (full_tile)
+            sel_tile<IO, DC, ACC, HAS_Z, SOFTPLUS, kFull>(xs, dts, zs, bc, A2, h, dsum, dsk, yp, D,
+                                                           C::T, half);
+        else
+            sel_tile<IO, DC, ACC, HAS_Z, SOFTPLUS, kRagged>(xs, dts, zs, bc, A2, h, dsum, dsk, yp,
+                                                             D, vd ? L - t0 : 0, half);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+
+        if (agg_pass && v == ntl - 1) {
+            constexpr int NC = 32 * C::CWARPS;
+            const size_t slot = size_t(cb) * S + s;
+            float2 carry[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = half * C::NH + 2 * q;
+                carry[q] = (vd && h0 != nullptr)
+                               ? make_float2(h0[(size_t(b) * D + d) * C::N + n],
+                                             h0[(size_t(b) * D + d) * C::N + n + 1])
+                               : make_float2(0.0f, 0.0f);
+            }
+            if (s > 0) {
+                float *ag = ws.agg + slot * C::kAgg * DC;
+                if (half == 0) ag[ch] = dsum;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int n = half * C::NH + 2 * q;
+                    ag[(1 + n) * DC + ch] = h[q].x;
+                    ag[(2 + n) * DC + ch] = h[q].y;
+                }
+                __threadfence();
+                named_bar_sync(1, NC);
+                if (tid == 0 && s != withheld) st_release_gpu(&ws.flags[slot], kFlagAggregate);
+                float acc_d = 0.0f;  // composition of splits sp+1 .. s-1
+                float2 acc_h[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc_h[q] = make_float2(0.0f, 0.0f);
+                bool done = false;
+                for (int sp = s - 1; sp >= 0 && !done; --sp) {
+                    const size_t sl = size_t(cb) * S + sp;
+                    if (tid == 0) *bcast = static_cast<int>(poll_flag(&ws.flags[sl], timeout_ns));
+                    named_bar_sync(1, NC);
+                    const int fv = *bcast;
+                    named_bar_sync(1, NC);
+                    if (fv == static_cast<int>(kFlagInclusive)) {
+                        const float *in = ws.incl + sl * C::kIncl * DC;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int n = half * C::NH + 2 * q;
+                            const float px = pow2_t<ACC>(A2[q].x * acc_d);
+                            const float py = pow2_t<ACC>(A2[q].y * acc_d);
+                            carry[q].x = fmaf(px, __ldcg(&in[n * DC + ch]), acc_h[q].x);
+                            carry[q].y = fmaf(py, __ldcg(&in[(n + 1) * DC + ch]), acc_h[q].y);
+                        }
+                        done = true;
+                    } else if (fv == static_cast<int>(kFlagAggregate)) {
+                        const float *ax = ws.agg + sl * C::kAgg * DC;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int n = half * C::NH + 2 * q;
+                            const float px = pow2_t<ACC>(A2[q].x * acc_d);
+                            const float py = pow2_t<ACC>(A2[q].y * acc_d);
+                            acc_h[q].x = fmaf(px, __ldcg(&ax[(1 + n) * DC + ch]), acc_h[q].x);
+                            acc_h[q].y = fmaf(py, __ldcg(&ax[(2 + n) * DC + ch]), acc_h[q].y);
+                        }
+                        acc_d += __ldcg(&ax[ch]);
+                    } else {
+                        if (tid == 0) report_status(LR_ERR_TIMEOUT);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) carry[q] = acc_h[q];
+                        done = true;
+                    }
+                }
+            }
+            float *in = ws.incl + slot * C::kIncl * DC;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int n = half * C::NH + 2 * q;
+                in[n * DC + ch] = fmaf(pow2_t<ACC>(A2[q].x * dsum), carry[q].x, h[q].x);
+                in[(n + 1) * DC + ch] = fmaf(pow2_t<ACC>(A2[q].y * dsum), carry[q].y, h[q].y);
+                h[q] = carry[q];
+            }
+            __threadfence();
+            named_bar_sync(1, NC);
+            if (tid == 0 && s != withheld) st_release_gpu(&ws.flags[slot], kFlagInclusive);
+        }
+    }
+    if (h_final != nullptr && vd && s == S - 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int n = half * C::NH + 2 * q;
+            h_final[(size_t(b) * D + d) * C::N + n] = h[q].x;
+            h_final[(size_t(b) * D + d) * C::N + n + 1] = h[q].y;
+        }
+    }
+}
+
+// ============================================================================
+// Host side
+// ============================================================================
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D map over a row-major (d2, d1, d0) tensor, box (b0, b1, 1), no swizzle,
+// zero fill outside the tensor.
+bool make_map_3d(CUtensorMap *tm, const void *base, CUtensorMapDataType type, size_t esize,
+                 uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(tm, type, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Per-device facts and per-kernel attributes, looked up once.
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    std::once_flag once;
+    int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Sets a kernel's dynamic shared-memory limit once per device and returns
+// how many of its blocks fit on one SM (0 on error).
+template <auto Kernel>
+int kernel_blocks_per_sm(int threads, size_t smem, int dev) {
+    static std::once_flag once[kMaxDevices];
+    static int blocks[kMaxDevices];
+    std::call_once(once[dev], [&] {
+        blocks[dev] = 0;
+        if (cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Kernel, threads, smem) == cudaSuccess)
+            blocks[dev] = n;
+    });
+    return blocks[dev];
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Splits are used only when the channel blocks alone leave most SMs idle; the
+// split count then targets every resident block slot.  Two splits would
+// only double the work per split, so fewer than three means one.
+void choose_splits(DiagPlan *p, int sms, int resident_per_sm, int agg_floats, int incl_floats) {
+    int S = 1;
+    if (g_split_override > 0) {
+        S = g_split_override;
+    } else if (p->n_cb * 2 < sms) {
+        const int64_t slots = int64_t(sms) * (resident_per_sm > 0 ? resident_per_sm : 1);
+        const int64_t want = (slots + p->n_cb - 1) / p->n_cb;
+        S = want >= 3 ? static_cast<int>(want < (1 << 20) ? want : (1 << 20)) : 1;
+    }
+    S = S < 1 ? 1 : (S > p->n_tiles ? p->n_tiles : S);
+    p->tps = (p->n_tiles + S - 1) / S;
+    p->S = (p->n_tiles + p->tps - 1) / p->tps;
+    if (p->S <= 1) {
+        p->S = 1;
+        p->tps = p->n_tiles;
+        p->ctrl_bytes = 0;
+        p->ws_bytes = 0;
+        return;
+    }
+    const size_t slots = size_t(p->n_cb) * p->S;
+    p->ctrl_bytes = align_up((slots + 1) * sizeof(uint32_t), 256);
+    const size_t agg = align_up(slots * agg_floats * p->dc * sizeof(float), 256);
+    const size_t incl = align_up(slots * incl_floats * p->dc * sizeof(float), 256);
+    p->ws_bytes = p->ctrl_bytes + agg + incl;
+}
+
+LookbackWs carve(const DiagPlan &p, void *workspace, int agg_floats) {
+    LookbackWs w{};
+    if (p.S <= 1) return w;
+    char *base = static_cast<char *>(workspace);
+    const size_t slots = size_t(p.n_cb) * p.S;
+    w.flags = reinterpret_cast<uint32_t *>(base);
+    w.ticket = w.flags + slots;
+    w.agg = reinterpret_cast<float *>(base + p.ctrl_bytes);
+    w.incl = reinterpret_cast<float *>(
+        base + p.ctrl_bytes + align_up(slots * agg_floats * p.dc * sizeof(float), 256));
+    return w;
+}
+
+uint64_t timeout_ns() {
+    return g_withheld_split >= 1 ? uint64_t(g_withheld_timeout_ms) * 1000000ull : kDefaultTimeoutNs;
+}
+
+constexpr int kSelDC = 32;
+
+int current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return LR_ERR_CUDA;
+    return LR_OK;
+}
+
+}  // namespace
+
+int device_sm_count(int *sms) {
+    int dev = 0;
+    if (current_device(&dev) != LR_OK) return LR_ERR_CUDA;
+    DeviceInfo &di = g_dev[dev];
+    std::call_once(di.once, [&] {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) di.sms = n;
+    });
+    if (di.sms <= 0) return LR_ERR_CUDA;
+    *sms = di.sms;
+    return LR_OK;
+}
+
+// ---------------------------------------------------------------- RG-LRU host
+template <typename IO, bool ACC>
+static int rglru_resident(int dev) {
+    return kernel_blocks_per_sm<rglru_scan_kernel<IO, ACC>>(RgCfg<IO>::THREADS, RgCfg<IO>::SMEM, dev);
+}
+
+int rglru_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p) {
+    int sms = 0, dev = 0;
+    if (device_sm_count(&sms) != LR_OK || current_device(&dev) != LR_OK) return LR_ERR_CUDA;
+    *p = DiagPlan{};
+    p->dc = RgCfg<float>::DC;
+    p->tile_t = RgCfg<float>::T;
+    p->n_cb = B * ((D + p->dc - 1) / p->dc);
+    p->n_tiles = static_cast<int>((L + p->tile_t - 1) / p->tile_t);
+    const int per_sm = io == LR_BF16 ? rglru_resident<__nv_bfloat16, false>(dev)
+                                     : rglru_resident<float, true>(dev);
+    if (per_sm <= 0) return LR_ERR_CUDA;
+    choose_splits(p, sms, per_sm, RgCfg<float>::kAgg, RgCfg<float>::kIncl);
+    return LR_OK;
+}
+
+template <typename IO, bool ACC>
+static int rglru_launch_t(const void *x, const void *r, const void *i, const float *a_log, float c,
+                          const float *h0, void *y, float *h_final, int64_t B, int64_t L,
+                          int64_t D, const DiagPlan &p, void *workspace, cudaStream_t stream) {
+    using C = RgCfg<IO>;
+    CUtensorMap mx, mr, mi;
+    const auto tt = Io<IO>::kTmType;
+    if (!make_map_3d(&mx, x, tt, sizeof(IO), D, L, B, C::DC, C::T) ||
+        !make_map_3d(&mr, r, tt, sizeof(IO), D, L, B, C::DC, C::T) ||
+        !make_map_3d(&mi, i, tt, sizeof(IO), D, L, B, C::DC, C::T))
+        return LR_ERR_CUDA;
+    if (p.S > 1 && cudaMemsetAsync(workspace, 0, p.ctrl_bytes, stream) != cudaSuccess)
+        return LR_ERR_CUDA;
+    const LookbackWs ws = carve(p, workspace, C::kAgg);
+    const int n_db = static_cast<int>((D + C::DC - 1) / C::DC);
+    const int64_t grid = p.n_cb * p.S;
+    rglru_scan_kernel<IO, ACC><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(
+        mx, mr, mi, a_log, c, h0, static_cast<IO *>(y), h_final, static_cast<int>(L),
+        static_cast<int>(D), n_db, p.S, p.tps, p.n_tiles, ws, g_withheld_split, timeout_ns());
+    return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+int rglru_launch(const void *x, const void *r, const void *i, const float *a_log, float c,
+                 const float *h0, void *y, float *h_final, int64_t B, int64_t L, int64_t D,
+                 lr_dtype io, const DiagPlan &p, void *workspace, cudaStream_t stream) {
+    if (io == LR_BF16)
+        return rglru_launch_t<__nv_bfloat16, false>(x, r, i, a_log, c, h0, y, h_final, B, L, D, p,
+                                                    workspace, stream);
+    return rglru_launch_t<float, true>(x, r, i, a_log, c, h0, y, h_final, B, L, D, p, workspace,
+                                       stream);
+}
+
+// ------------------------------------------------------------- selective host
+template <typename IO, bool ACC, bool HZ, bool SP>
+static int selective_resident(int dev) {
+    using C = SelCfg<IO, kSelDC>;
+    return kernel_blocks_per_sm<selective_scan_kernel<IO, kSelDC, ACC, HZ, SP>>(C::THREADS, C::SMEM,
+                                                                               dev);
+}
+
+template <typename IO, bool ACC>
+static int selective_resident_any(int dev, bool hz, bool sp) {
+    // all four variants share block size and shared memory; each needs its
+    // own dynamic shared-memory attribute, so every one is set up here
+    const int a = selective_resident<IO, ACC, true, true>(dev);
+    const int b = selective_resident<IO, ACC, true, false>(dev);
+    const int c = selective_resident<IO, ACC, false, true>(dev);
+    const int d = selective_resident<IO, ACC, false, false>(dev);
+    return hz ? (sp ? a : b) : (sp ? c : d);
+}
+
+int selective_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p) {
+    int sms = 0, dev = 0;
+    if (device_sm_count(&sms) != LR_OK || current_device(&dev) != LR_OK) return LR_ERR_CUDA;
+    *p = DiagPlan{};
+    p->dc = kSelDC;
+    p->tile_t = SelCfg<float, kSelDC>::T;
+    p->n_cb = B * ((D + p->dc - 1) / p->dc);
+    p->n_tiles = static_cast<int>((L + p->tile_t - 1) / p->tile_t);
+    const int per_sm = io == LR_BF16 ? selective_resident_any<__nv_bfloat16, false>(dev, true, true)
+                                     : selective_resident_any<float, true>(dev, true, true);
+    if (per_sm <= 0) return LR_ERR_CUDA;
+    choose_splits(p, sms, per_sm, SelCfg<float, kSelDC>::kAgg, SelCfg<float, kSelDC>::kIncl);
+    return LR_OK;
+}
+
+template <typename IO, bool ACC, bool HZ, bool SP>
+static int selective_launch_v(const CUtensorMap &mx, const CUtensorMap &mdt, const CUtensorMap &mz,
+                              const CUtensorMap &mB, const CUtensorMap &mC, const float *A_log,
+                              const float *Dskip, const float *h0, void *y, float *h_final,
+                              int64_t L, int64_t D, const DiagPlan &p, const LookbackWs &ws,
+                              cudaStream_t stream) {
+    using C = SelCfg<IO, kSelDC>;
+    const int n_db = static_cast<int>((D + C::DC - 1) / C::DC);
+    const int64_t grid = p.n_cb * p.S;
+    selective_scan_kernel<IO, kSelDC, ACC, HZ, SP>
+        <<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(
+            mx, mdt, mz, mB, mC, A_log, Dskip, h0, static_cast<IO *>(y), h_final,
+            static_cast<int>(L), static_cast<int>(D), n_db, p.S, p.tps, p.n_tiles, ws,
+            g_withheld_split, timeout_ns());
+    return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+template <typename IO, bool ACC>
+static int selective_launch_t(const void *x, const void *dt, const void *z, const void *Bm,
+                              const void *Cm, const float *A_log, const float *Dskip,
+                              const float *h0, void *y, float *h_final, int64_t B, int64_t L,
+                              int64_t D, int dt_softplus, const DiagPlan &p, void *workspace,
+                              cudaStream_t stream) {
+    using C = SelCfg<IO, kSelDC>;
+    CUtensorMap mx, mdt, mz, mB, mC;
+    const auto tt = Io<IO>::kTmType;
+    if (!make_map_3d(&mx, x, tt, sizeof(IO), D, L, B, C::DC, C::T) ||
+        !make_map_3d(&mdt, dt, tt, sizeof(IO), D, L, B, C::DC, C::T) ||
+        !make_map_3d(&mz, z != nullptr ? z : x, tt, sizeof(IO), D, L, B, C::DC, C::T) ||
+        !make_map_3d(&mB, Bm, tt, sizeof(IO), C::N, L, B, C::N, C::T) ||
+        !make_map_3d(&mC, Cm, tt, sizeof(IO), C::N, L, B, C::N, C::T))
+        return LR_ERR_CUDA;
+    if (p.S > 1 && cudaMemsetAsync(workspace, 0, p.ctrl_bytes, stream) != cudaSuccess)
+        return LR_ERR_CUDA;
+    const LookbackWs ws = carve(p, workspace, C::kAgg);
+    const bool hz = z != nullptr, sp = dt_softplus != 0;
+    if (hz && sp)
+        return selective_launch_v<IO, ACC, true, true>(mx, mdt, mz, mB, mC, A_log, Dskip, h0, y,
+                                                       h_final, L, D, p, ws, stream);
+    if (hz)
+        return selective_launch_v<IO, ACC, true, false>(mx, mdt, mz, mB, mC, A_log, Dskip, h0, y,
+                                                        h_final, L, D, p, ws, stream);
+    if (sp)
+        return selective_launch_v<IO, ACC, false, true>(mx, mdt, mz, mB, mC, A_log, Dskip, h0, y,
+                                                        h_final, L, D, p, ws, stream);
+    return selective_launch_v<IO, ACC, false, false>(mx, mdt, mz, mB, mC, A_log, Dskip, h0, y,
+                                                     h_final, L, D, p, ws, stream);
+}
+
+int selective_launch(const void *x, const void *dt, const void *z, const void *Bm, const void *Cm,
+                     const float *A_log, const float *Dskip, const float *h0, void *y,
+                     float *h_final, int64_t B, int64_t L, int64_t D, lr_dtype io, int dt_softplus,
+                     const DiagPlan &p, void *workspace, cudaStream_t stream) {
+    if (io == LR_BF16)
+        return selective_launch_t<__nv_bfloat16, false>(x, dt, z, Bm, Cm, A_log, Dskip, h0, y,
+                                                        h_final, B, L, D, dt_softplus, p,
+                                                        workspace, stream);
+    return selective_launch_t<float, true>(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D,
+                                           dt_softplus, p, workspace, stream);
+}
+
+int diag_status_read_and_clear(int *status) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_diag_status, sizeof(int)) != cudaSuccess) return LR_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_diag_status, &zero, sizeof(int)) != cudaSuccess)
+            return LR_ERR_CUDA;
+    }
+    *status = v;
+    return LR_OK;
+}
+
+}  // namespace lr

@@ -1,0 +1,58 @@
+// lr_internal.h -- host-side declarations shared by the library's .cu files.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime.h>
+
+#include "lrscan.h"
+
+namespace lr {
+
+// Work decomposition of a diagonal scan (selective or RG-LRU).
+//   n_cb   channel blocks (batch x ceil(D / DC)); one thread block each when S == 1
+//   S      time splits per channel block (S > 1: decoupled look-back between splits)
+//   tps    tiles per split; n_tiles = ceil(L / T)
+struct DiagPlan {
+    int64_t n_cb = 0;
+    int S = 1;
+    int tps = 0;
+    int n_tiles = 0;
+    int dc = 0;           // channels per thread block
+    int tile_t = 0;       // time steps per tile
+    size_t ctrl_bytes = 0;  // flags + ticket (cleared at each call)
+    size_t ws_bytes = 0;    // total workspace
+};
+
+// Process-wide knobs (see lr_set_split_override / lr_test_withhold_split).
+extern int g_split_override;
+extern int g_withheld_split;
+extern int g_withheld_timeout_ms;
+
+// Default wall-clock limit of every bounded device-side wait.
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s
+
+int device_sm_count(int *sms);  // LR_OK / LR_ERR_CUDA
+
+int rglru_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p);
+int rglru_launch(const void *x, const void *r, const void *i, const float *a_log, float c,
+                 const float *h0, void *y, float *h_final, int64_t B, int64_t L, int64_t D,
+                 lr_dtype io, const DiagPlan &p, void *workspace, cudaStream_t stream);
+
+int selective_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p);
+int selective_launch(const void *x, const void *dt, const void *z, const void *Bm,
+                     const void *Cm, const float *A_log, const float *Dskip, const float *h0,
+                     void *y, float *h_final, int64_t B, int64_t L, int64_t D, lr_dtype io,
+                     int dt_softplus, const DiagPlan &p, void *workspace, cudaStream_t stream);
+
+int diag_status_read_and_clear(int *status);
+
+// HGRN2 (chunked tcgen05 kernel)
+int hgrn2_workspace(int64_t B, int64_t L, int64_t H, size_t *bytes);
+int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
+                 void *o, float *S_final, int64_t B, int64_t L, int64_t H, void *workspace,
+                 cudaStream_t stream);
+int hgrn2_status_read_and_clear(int *status);
+
+}  // namespace lr

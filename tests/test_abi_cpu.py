@@ -1,0 +1,152 @@
+"""The C-ABI library loads, exports every symbol include/lrscan.h declares,
+and rejects bad arguments before any CUDA call.
+
+No test here launches anything: every call carries at least one invalid
+argument, which the library's host-side validation catches first, so fake
+pointers are never dereferenced.  Runs without a GPU.
+"""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lrscan.h")
+
+
+@pytest.fixture(scope="module")
+def lr():
+    from selective_state_space_chunked_gb300 import build
+    build.build()
+    from selective_state_space_chunked_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lr_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_scans():
+    names = declared_functions()
+    for n in ("lr_selective_scan_fwd", "lr_rglru_scan_fwd", "lr_hgrn2_fwd",
+              "lr_check_status", "lr_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lr):
+    import ctypes
+    so = ctypes.CDLL(lr.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+    assert set(declared_functions()) == set(lr.SIGNATURES)
+
+
+def test_status_strings_and_version(lr):
+    assert lr.lr_status_string(0) == "LR_OK"
+    for code in range(-7, 0):
+        assert lr.lr_status_string(code).startswith("LR_ERR_")
+    assert lr.lr_status_string(-99) == "unknown lrscan status"
+    assert lr.lr_version() >= 10000
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced (validation fails first)
+
+
+def sel_args(**kw):
+    a = dict(x=FAKE, dt=FAKE, z=FAKE, Bm=FAKE, Cm=FAKE, A_log=FAKE, Dskip=FAKE,
+             h0=FAKE, y=FAKE, h_final=FAKE, B=2, L=64, D=64, N=16, io=1,
+             dt_softplus=1, workspace=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return a
+
+
+def call_sel(lr, **kw):
+    a = sel_args(**kw)
+    return lr.lr_selective_scan_fwd(*a.values())
+
+
+@pytest.mark.parametrize("field", ["x", "dt", "Bm", "Cm", "A_log", "y"])
+def test_selective_null_required_pointer(lr, field):
+    assert call_sel(lr, **{field: None}) == lr.LR_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), -1), (dict(L=-5), -1), (dict(D=-8), -1), (dict(io=7), -1),
+    (dict(N=8), -2), (dict(D=60), -2), (dict(D=66, io=0), -2),
+    (dict(L=1 << 40), -2),
+    (dict(x=FAKE + 4), -3), (dict(Cm=FAKE + 8), -3), (dict(h0=FAKE + 2), -3),
+    (dict(h_final=FAKE + 12), -3), (dict(z=FAKE + 1), -3),
+])
+def test_selective_validation_codes(lr, kw, code):
+    assert call_sel(lr, **kw) == code
+
+
+def rg_args(**kw):
+    a = dict(x=FAKE, r=FAKE, i=FAKE, a_log=FAKE, c=8.0, h0=FAKE, y=FAKE,
+             h_final=FAKE, B=2, L=64, D=64, io=1, workspace=None, ws_bytes=0,
+             stream=None)
+    a.update(kw)
+    return a
+
+
+def call_rg(lr, **kw):
+    return lr.lr_rglru_scan_fwd(*rg_args(**kw).values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), -1), (dict(r=None), -1), (dict(i=None), -1),
+    (dict(a_log=None), -1), (dict(y=None), -1), (dict(c=float("nan")), -1),
+    (dict(c=float("inf")), -1), (dict(B=-1), -1), (dict(io=2), -1),
+    (dict(D=12), -2), (dict(D=6, io=0), -2),
+    (dict(r=FAKE + 8), -3), (dict(a_log=FAKE + 4), -3),
+])
+def test_rglru_validation_codes(lr, kw, code):
+    assert call_rg(lr, **kw) == code
+
+
+def hg_args(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, S0=FAKE, o=FAKE, S_final=FAKE,
+             B=2, L=64, H=4, dk=128, dv=128, chunk=64, io=1, workspace=None,
+             ws_bytes=0, stream=None)
+    a.update(kw)
+    return a
+
+
+def call_hg(lr, **kw):
+    return lr.lr_hgrn2_fwd(*hg_args(**kw).values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(g=None), -1), (dict(o=None), -1),
+    (dict(H=0), -1), (dict(dk=0), -1), (dict(chunk=0), -1), (dict(B=-2), -1),
+    (dict(dk=64), -2), (dict(dv=96), -2), (dict(chunk=32), -2), (dict(io=0), -2),
+    (dict(k=FAKE + 2), -3), (dict(S0=FAKE + 4), -3),
+])
+def test_hgrn2_validation_codes(lr, kw, code):
+    assert call_hg(lr, **kw) == code
+
+
+def test_workspace_size_degenerate_shapes_need_nothing(lr):
+    assert lr.lr_selective_scan_workspace_size(0, 10, 64, 16, 1) == 0
+    assert lr.lr_selective_scan_workspace_size(1, 10, 64, 8, 1) == 0
+    assert lr.lr_rglru_scan_workspace_size(1, 0, 64, 1) == 0
+    assert lr.lr_hgrn2_workspace_size(1, 0, 2, 128, 128, 1) == 0
+
+
+def test_hidden_not_divisible_by_heads_raises_value_error(lr):
+    import torch
+    q = torch.zeros(1, 4, 100, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        lr.hgrn2(q, q, q, q, H=3)
+
+
+def test_package_has_no_cpu_fallback():
+    """The product package never imports the oracle."""
+    pkg = os.path.join(ROOT, "selective_state_space_chunked_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
