@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the gated linear-recurrence scans on one node.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the RG-LRU scan at B=8, L=4096, D=2560 (bf16 I/O), the selective SSM scan at
+B=4, L=16384, d_inner=4096, N=16 (bf16 I/O) and, when built, the HGRN2
+recurrence at B=4, L=4096, 16 heads x 128 (bf16 I/O).  The metric is
+token-channel steps per second over the step (B*L*channels summed over the
+scans, HGRN2 counting its output channels), with per-scan GB/s, % of the
+measured HBM peak and, for HGRN2, TFLOP/s and tensor utilisation.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 the script runs under torch.distributed.run, one rank per GPU;
+every rank runs the same per-rank workload (independent replicas, weak
+scaling) and rank 0 prints one JSON line with the whole-job throughput
+(the units all ranks processed over the slowest rank's time).
+
+``--impl reference`` times the float64 CPU oracle (the correctness
+reference, never tuned) on the host cores on a bounded sample of the same
+workload and prints the same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from selective_state_space_chunked_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "scan tok·ch/s"
+UNIT = "tok·ch/s"
+
+
+# ----------------------------------------------------------------------------
+# workload bookkeeping (algorithmic bytes / flops per launch)
+# ----------------------------------------------------------------------------
+def algorithmic(cfg: wl.Config) -> dict:
+    """Bytes a launch must move (inputs read once, outputs written once) and
+    the tensor-core flops of HGRN2's chunked form."""
+    es = 2 if cfg.io == "bf16" else 4
+    B, L, D = cfg.B, cfg.L, cfg.D
+    if cfg.form == "rglru":
+        by = 4 * es * B * L * D + 4 * D + (2 * 4 * B * D if cfg.with_h0 else 4 * B * D)
+        return {"bytes": by, "flops": 0, "units": B * L * D}
+    if cfg.form == "selective":
+        N = cfg.N
+        by = (4 * es * B * L * D + 2 * es * B * L * N + 4 * D * N + 4 * D
+              + (2 if cfg.with_h0 else 1) * 4 * B * D * N)
+        return {"bytes": by, "flops": 0, "units": B * L * D}
+    d = cfg.head_dim
+    by = 5 * es * B * L * cfg.H * d + 4 * B * cfg.H * d * d
+    # per token and head: QK^T and P V over the chunk (2*C*d each), Q S^T and
+    # the state update (2*d*d each)
+    fl = B * L * cfg.H * (4 * cfg.chunk * d + 4 * d * d)
+    return {"bytes": by, "flops": fl, "units": B * L * cfg.H * d}
+
+
+# The scans one step runs (the workloads the pages' layers are sized for).
+STEP_CONFIGS = (2, 3)
+
+
+def step_configs():
+    return [wl.CONFIGS[k] for k in STEP_CONFIGS]
+
+
+# ----------------------------------------------------------------------------
+# clocks sampling (nvidia-smi during the timed region)
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers
+# ----------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (bounded samples of the same workloads)
+# ----------------------------------------------------------------------------
+def oracle_sample(cfg: wl.Config):
+    """A bounded slice of a workload for the CPU oracle: whole sequences of a
+    subset of channels (RG-LRU, selective) or heads (HGRN2) of batch row 0."""
+    if cfg.form == "rglru":
+        p = wl.make_inputs(cfg, B=1)
+        ch = 1024
+        return ("rglru", dict(x=p["x"][:, :, :ch], r=p["r"][:, :, :ch], i=p["i"][:, :, :ch],
+                              a_log=p["a_log"][:ch], c=p["c"],
+                              h0=None if p["h0"] is None else p["h0"][:, :ch]),
+                cfg.L * ch)
+    if cfg.form == "selective":
+        p = wl.make_inputs(cfg, B=1)
+        ch = 256
+        return ("selective", dict(x=p["x"][:, :, :ch], dt=p["dt"][:, :, :ch],
+                                  z=p["z"][:, :, :ch], Bm=p["Bm"], Cm=p["Cm"],
+                                  A_log=p["A_log"][:ch], Dskip=p["Dskip"][:ch],
+                                  h0=None if p["h0"] is None else p["h0"][:, :ch]),
+                cfg.L * ch)
+    p = wl.make_inputs(cfg, B=1)
+    heads = cfg.H
+    hd = cfg.head_dim
+    sl = slice(0, heads * hd)
+    return ("hgrn2", dict(q=p["q"][:, :, sl], k=p["k"][:, :, sl], v=p["v"][:, :, sl],
+                          g=p["g"][:, :, sl], H=heads), cfg.L * heads * hd)
+
+
+def run_oracle(kind, args, threads=0):
+    import oracle
+    if kind == "rglru":
+        return oracle.rglru_scan(**args, threads=threads)
+    if kind == "selective":
+        return oracle.selective_scan(**args, threads=threads)
+    return oracle.hgrn2(**args, threads=threads)
+
+
+def cpu_baseline(cfgs, repeats=1, samples=None) -> dict:
+    """Times the oracle on each workload's sample; the step-equivalent rate is
+    total units / sum over scans of (units / sampled rate)."""
+    import oracle
+    cores = oracle.max_threads()
+    if samples is None:
+        samples = [(cfg, *oracle_sample(cfg)) for cfg in cfgs]
+    rates = {}
+    for cfg, kind, args, units in samples:
+        run_oracle(kind, args)  # warm (page-in, thread pool)
+        t0 = time.perf_counter()
+        for _ in range(repeats):
+            run_oracle(kind, args)
+        dt = (time.perf_counter() - t0) / repeats
+        rates[cfg.name] = units / dt
+    total_units = sum(algorithmic(c)["units"] for c in cfgs)
+    step_time = sum(algorithmic(c)["units"] / rates[c.name] for c in cfgs)
+    desc = "; ".join(f"{c.name}: {u} of {algorithmic(c)['units']} units"
+                     for c, _, _, u in samples)
+    return {"value": total_units / step_time, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "whole sequences of a channel/head subset of batch row 0 -- " + desc,
+            "per_scan_units_per_s": rates}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def make_call(lr, cfg, p):
+    if cfg.form == "rglru":
+        return lambda: lr.rglru_scan(p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"])
+    if cfg.form == "selective":
+        return lambda: lr.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], p["A_log"],
+                                         z=p["z"], Dskip=p["Dskip"], h0=p["h0"])
+    return lambda: lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=p["H"])
+
+
+def input_bytes(p) -> int:
+    return sum(t.numel() * t.element_size() for t in p.values() if torch.is_tensor(t))
+
+
+def gpu_arm(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    from selective_state_space_chunked_gb300 import binding as lr
+    cfgs = step_configs()
+    inputs = [wl.make_inputs(c, device=dev) for c in cfgs]
+    calls = [make_call(lr, c, p) for c, p in zip(cfgs, inputs)]
+    alg = [algorithmic(c) for c in cfgs]
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        for fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    if lr.lr_check_status(stream.cuda_stream) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in cfgs] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for k in range(args.steps):
+        for j, fn in enumerate(calls):
+            ev[k][j][0].record(stream)
+            fn()
+            ev[k][j][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if rank == 0 else None
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    status = lr.lr_check_status(stream.cuda_stream)
+    if status != 0:
+        raise RuntimeError(f"device status {lr.lr_status_string(status)}")
+
+    per_scan = []
+    for j, c in enumerate(cfgs):
+        ms = statistics.mean(ev[k][j][0].elapsed_time(ev[k][j][1]) for k in range(args.steps))
+        a = alg[j]
+        d = {"workload": c.name, "ms": ms, "tok_ch_per_s": a["units"] / (ms * 1e-3),
+             "gb_per_s": a["bytes"] / (ms * 1e-3) / 1e9}
+        if a["flops"]:
+            d["tflop_per_s"] = a["flops"] / (ms * 1e-3) / 1e12
+        per_scan.append(d)
+
+    # end-to-end through the public API with host buffers: pinned host inputs,
+    # the library copies them in, runs, copies outputs back and synchronises
+    host_inputs = [{k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in p.items()}
+                   for p in inputs]
+    host_calls = [make_call(lr, c, p) for c, p in zip(cfgs, host_inputs)]
+    h2d = sum(input_bytes(p) for p in host_inputs)
+    for fn in host_calls:
+        fn()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier(world)
+    t0 = time.perf_counter()
+    d2h = 0
+    for _ in range(e2e_steps):
+        d2h = 0
+        for fn in host_calls:
+            outs = fn()
+            d2h += sum(t.numel() * t.element_size() for t in outs)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev) / e2e_steps
+    del host_inputs, host_calls
+
+    units_step = sum(a["units"] for a in alg)
+    value = world * units_step * args.steps / (total_ms * 1e-3)
+    peaks = load_peaks()
+    dom = max(range(len(cfgs)), key=lambda j: per_scan[j]["ms"])
+    roof = {"kernel": cfgs[dom].name, "bound": "hbm", "achieved": per_scan[dom]["gb_per_s"],
+            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": per_scan[dom]["gb_per_s"] / peaks["hbm_gbs"],
+            "traffic": traffic_for(cfgs[dom].name), "peak_source": peaks["source"]}
+    for d in per_scan:
+        d["hbm_frac"] = d["gb_per_s"] / peaks["hbm_gbs"]
+        if "tflop_per_s" in d:
+            d["tensor_frac"] = d["tflop_per_s"] / peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic (seeded generators with the pages' layer distributions)",
+        "config": {"workload": " + ".join(c.name for c in cfgs),
+                   "l2": "inputs larger than L2 (129 MB) on every launch, no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "per_scan": per_scan,
+        "roofline": roof,
+        "e2e": {"value": world * units_step / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": len(cfgs) * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfgs)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def kernel_source_digest() -> str:
+    """Digest of the library's CUDA sources: a stored ncu traffic figure is
+    used only while the kernels it was taken from are unchanged."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_chunked_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(name: str):
+    """DRAM read+write bytes per full-size launch from the committed ncu
+    summary (profiles/traffic.json), or None when it is missing or was taken
+    from kernels that have changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_digest") != kernel_source_digest():
+        return None
+    return d.get("per_launch_bytes", {}).get(name)
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the oracle on host cores
+# ----------------------------------------------------------------------------
+def reference_arm(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cfgs = step_configs()
+    samples = [(cfg, *oracle_sample(cfg)) for cfg in cfgs]
+    cb = None
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(cfgs, samples=samples)
+    for _ in range(args.steps):
+        cb = cpu_baseline(cfgs, samples=samples)
+        vals.append(cb["value"])
+    value = statistics.mean(vals)
+    cb["value"] = value
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sum(algorithmic(c)["units"] for c in cfgs) / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generators with the pages' layer distributions)",
+        "config": {"workload": " + ".join(c.name for c in cfgs),
+                   "l2": "n/a (host cores)", "parallelism": "host threads"},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip timing the CPU oracle beside the GPU arm")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()
