@@ -146,6 +146,36 @@ int lr_rglru_scan_fwd(const void *x, const void *r, const void *i,
                       int64_t B, int64_t L, int64_t D, lr_dtype io,
                       void *workspace, size_t ws_bytes, lr_stream_t stream);
 
+/*
+ * RG-LRU scan for callers that cannot allocate device memory.  The source
+ * pages have no counterpart; this entry point exists for the library's
+ * users.  Some host frameworks and runtimes own every byte of device memory
+ * through their own allocator or fix their memory budget at start-up, and
+ * some latency-critical paths cannot afford cudaMalloc's implicit device
+ * synchronisation; such callers have no way to provide the workspace that
+ * lr_rglru_scan_fwd may need.
+ *
+ * Same arguments, arithmetic, layouts and results as lr_rglru_scan_fwd, minus
+ * the workspace: the look-back scratch comes from a fixed array of 1 MiB
+ * (1048576 bytes) built into the library, which every GPU that loads the
+ * library holds until the process exits.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - A problem whose look-back state would exceed 1 MiB is rejected with
+ *     LR_ERR_WORKSPACE before anything is launched (automatic splitting never
+ *     needs more than about 0.4 MiB; only a large lr_set_split_override can).
+ *   - All calls on a device share the array and it keeps the previous call's
+ *     contents; each call clears the part that must start at zero.  Calls
+ *     that overlap in time on the GPU (different streams) race on it and must
+ *     be serialised by the caller.
+ */
+int lr_rglru_scan_fwd_noalloc(const void *x, const void *r, const void *i,
+                              const float *a_log, float c, const float *h0,
+                              void *y, float *h_final,
+                              int64_t B, int64_t L, int64_t D, lr_dtype io,
+                              lr_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* HGRN2 matrix-state recurrence                                             */
 /* ------------------------------------------------------------------------ */

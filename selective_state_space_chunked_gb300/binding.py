@@ -44,6 +44,8 @@ SIGNATURES = {
     "lr_rglru_scan_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
     "lr_rglru_scan_fwd": (_I, [_P, _P, _P, _P, _F, _P, _P, _P,
                                _I64, _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_rglru_scan_fwd_noalloc": (_I, [_P, _P, _P, _P, _F, _P, _P, _P,
+                                       _I64, _I64, _I64, _I, _P]),
     "lr_hgrn2_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I]),
     "lr_hgrn2_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                           _I64, _I64, _I, _P, _SZ, _P]),
@@ -118,6 +120,13 @@ def lr_rglru_scan_fwd(x, r, i, a_log, c, h0, y, h_final, B, L, D, io,
                       workspace, ws_bytes, stream) -> int:
     return int(_lib.lr_rglru_scan_fwd(x, r, i, a_log, c, h0, y, h_final, B, L, D,
                                       io, workspace, ws_bytes, stream))
+
+
+def lr_rglru_scan_fwd_noalloc(x, r, i, a_log, c, h0, y, h_final, B, L, D, io,
+                              stream) -> int:
+    """RG-LRU scan using the library's built-in scratch (no workspace)."""
+    return int(_lib.lr_rglru_scan_fwd_noalloc(x, r, i, a_log, c, h0, y, h_final, B, L,
+                                              D, io, stream))
 
 
 def lr_hgrn2_workspace_size(B, L, H, dk, dv, io) -> int:

@@ -178,6 +178,25 @@ int lr_rglru_scan_fwd(const void *x, const void *r, const void *i, const float *
     return lr::rglru_launch(x, r, i, a_log, c, h0, y, h_final, B, L, D, io, p, workspace, st);
 }
 
+// RG-LRU scan without a caller workspace: same arithmetic and launch as
+// lr_rglru_scan_fwd, with the look-back scratch taken from the library's
+// built-in array.  Allocates nothing.
+int lr_rglru_scan_fwd_noalloc(const void *x, const void *r, const void *i, const float *a_log,
+                              float c, const float *h0, void *y, float *h_final, int64_t B,
+                              int64_t L, int64_t D, lr_dtype io, lr_stream_t stream) {
+    int rc = validate_rglru(x, r, i, a_log, c, h0, y, h_final, B, L, D, io);
+    if (rc != LR_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return LR_OK;
+    if (L == 0) return copy_state(h0, h_final, size_t(B) * D, st);
+    lr::DiagPlan p;
+    if ((rc = lr::rglru_plan(B, L, D, io, &p)) != LR_OK) return rc;
+    if (p.ws_bytes > lr::kRglruScratchBytes) return LR_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (p.ws_bytes > 0 && (rc = lr::rglru_builtin_scratch(&scratch)) != LR_OK) return rc;
+    return lr::rglru_launch(x, r, i, a_log, c, h0, y, h_final, B, L, D, io, p, scratch, st);
+}
+
 // ---------------------------------------------------------------- HGRN2
 size_t lr_hgrn2_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
                                lr_dtype io) {

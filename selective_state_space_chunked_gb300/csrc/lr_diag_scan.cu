@@ -981,6 +981,30 @@ int selective_launch(const void *x, const void *dt, const void *z, const void *B
                                            dt_softplus, p, workspace, stream);
 }
 
+// ---------------------------------------------------- built-in scratch (RG-LRU)
+// Scratch for lr_rglru_scan_fwd_noalloc: the look-back flags, ticket and split
+// descriptors of the RG-LRU scan live in this fixed array instead of a
+// caller-provided workspace.  Every GPU that loads the library holds it until
+// the process exits; all calls on a device share it.
+static __device__ __align__(256) unsigned char g_rglru_scratch[kRglruScratchBytes];
+
+int rglru_builtin_scratch(void **ptr) {
+    int dev = 0;
+    if (current_device(&dev) != LR_OK) return LR_ERR_CUDA;
+    static std::once_flag once[kMaxDevices];
+    static void *addr[kMaxDevices];
+    static cudaError_t err[kMaxDevices];
+    // Host code sees the array only through a stand-in symbol: its device
+    // address is looked up once per device, with that device current.
+    std::call_once(once[dev], [&] {
+        addr[dev] = nullptr;
+        err[dev] = cudaGetSymbolAddress(&addr[dev], g_rglru_scratch);
+    });
+    if (err[dev] != cudaSuccess || addr[dev] == nullptr) return LR_ERR_CUDA;
+    *ptr = addr[dev];
+    return LR_OK;
+}
+
 int diag_status_read_and_clear(int *status) {
     int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_diag_status, sizeof(int)) != cudaSuccess) return LR_ERR_CUDA;

@@ -48,6 +48,10 @@ int selective_launch(const void *x, const void *dt, const void *z, const void *B
 
 int diag_status_read_and_clear(int *status);
 
+// Built-in scratch of lr_rglru_scan_fwd_noalloc (1 MiB per device).
+constexpr size_t kRglruScratchBytes = size_t(1) << 20;
+int rglru_builtin_scratch(void **ptr);  // device address, set up once per device
+
 // HGRN2 (chunked tcgen05 kernel)
 int hgrn2_workspace(int64_t B, int64_t L, int64_t H, size_t *bytes);
 int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
