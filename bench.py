@@ -3,8 +3,8 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
 the RG-LRU scan at B=8, L=4096, D=2560 (bf16 I/O), the selective SSM scan at
-B=4, L=16384, d_inner=4096, N=16 (bf16 I/O) and, when built, the HGRN2
-recurrence at B=4, L=4096, 16 heads x 128 (bf16 I/O).  The metric is
+B=4, L=16384, d_inner=4096, N=16 (bf16 I/O) and the HGRN2 recurrence at
+B=4, L=4096, 16 heads x 128 (bf16 I/O).  The metric is
 token-channel steps per second over the step (B*L*channels summed over the
 scans, HGRN2 counting its output channels), with per-scan GB/s, % of the
 measured HBM peak and, for HGRN2, TFLOP/s and tensor utilisation.
@@ -68,7 +68,7 @@ def algorithmic(cfg: wl.Config) -> dict:
 
 
 # The scans one step runs (the workloads the pages' layers are sized for).
-STEP_CONFIGS = (2, 3)
+STEP_CONFIGS = (2, 3, 4)
 
 
 def step_configs():

@@ -194,8 +194,10 @@ int lr_rglru_scan_fwd_noalloc(const void *x, const void *r, const void *i,
  *          S0, S_final: (B, H, dv, dk) fp32.  Optional: S0, S_final.
  * Requirements: H > 0; dk == dv == 128; chunk == 64; io == LR_BF16; else
  *          LR_ERR_UNSUPPORTED.  Within every chunk of 64 steps the product
- *          of a channel's gates must stay above e^-160 (always true when
- *          g >= 0.09); otherwise the kernel sets LR_ERR_RANGE.
+ *          of a channel's gates must stay above 2^-160 (always true when
+ *          g >= 0.18, e.g. with a lower bound of 0.2); otherwise the kernel
+ *          sets LR_ERR_RANGE and that chunk's outputs are not meaningful.
+ * No workspace is needed (lr_hgrn2_workspace_size returns 0).
  */
 size_t lr_hgrn2_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk,
                                int64_t dv, lr_dtype io);

@@ -1,0 +1,104 @@
+"""Parity of the CUDA HGRN2 chunked tcgen05 kernel with the float64 oracle.
+
+Metric: max|gpu - ref| / max|ref| on o and on the final state separately,
+at most 1e-2 (bf16 I/O).  Oracle-sized cases cover several chunks, ragged
+sequence ends, a carried initial state and several heads; the full-size
+workload (B=4, L=4096, 16 heads of 128) runs in the benchmark's launch and is
+checked on sampled heads (the oracle computes heads independently).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import rel_err
+from selective_state_space_chunked_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def lr():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_chunked_gb300 import build
+    build.build()
+    from selective_state_space_chunked_gb300 import binding
+    binding.lr_set_split_override(0)
+    binding.lr_test_withhold_split(-1, 1000)
+    return binding
+
+
+def run(lr, p, S0=None):
+    q, k, v, g = (p[n].cuda() for n in ("q", "k", "v", "g"))
+    o, Sf = lr.hgrn2(q, k, v, g, H=p["H"], S0=None if S0 is None else S0.cuda())
+    torch.cuda.synchronize()
+    assert lr.lr_check_status(0) == 0
+    return o.float().cpu(), Sf.cpu()
+
+
+def check(lr, p, S0=None):
+    o, Sf = run(lr, p, S0)
+    orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], p["H"], S0=S0)
+    assert rel_err(o, orf) <= TOL, rel_err(o, orf)
+    assert rel_err(Sf, Srf) <= TOL, rel_err(Sf, Srf)
+
+
+@pytest.mark.parametrize("B,L,H", [(1, 256, 2), (2, 130, 1), (1, 64, 3), (1, 1, 1), (1, 63, 2),
+                                   (1, 1000, 2)])
+def test_hgrn2_oracle_sized(lr, B, L, H):
+    p = wl.hgrn2_inputs(B, L, H, 128, seed=B * 100 + L + H)
+    check(lr, p)
+
+
+def test_hgrn2_initial_state(lr):
+    p = wl.hgrn2_inputs(2, 200, 2, 128, seed=7, with_S0=True)
+    check(lr, p, S0=0.1 * p["S0"])
+
+
+def test_hgrn2_slow_and_fast_gates(lr):
+    """Gates near 1 (long memory) and near the 0.2 lower bound in one run."""
+    p = wl.hgrn2_inputs(1, 320, 2, 128, seed=8)
+    g = p["g"].float()
+    g[..., :128] = 0.999
+    g[..., 128:] = 0.2
+    p["g"] = g.to(torch.bfloat16)
+    check(lr, p)
+
+
+def test_hgrn2_split_resume(lr):
+    p = {k: (v.cuda() if torch.is_tensor(v) else v)
+         for k, v in wl.hgrn2_inputs(1, 512, 2, 128, seed=9).items()}
+    o, Sf = lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=2)
+    o1, S1 = lr.hgrn2(p["q"][:, :192], p["k"][:, :192], p["v"][:, :192], p["g"][:, :192], H=2)
+    o2, S2 = lr.hgrn2(p["q"][:, 192:], p["k"][:, 192:], p["v"][:, 192:], p["g"][:, 192:], H=2,
+                      S0=S1)
+    torch.cuda.synchronize()
+    assert rel_err(torch.cat([o1, o2], 1).float().cpu(), o.float().cpu()) <= 1e-2
+    assert rel_err(S2.cpu(), Sf.cpu()) <= 1e-2
+
+
+def test_hgrn2_gate_spread_beyond_range_is_reported(lr):
+    """A chunk whose gates multiply below 2^-160 sets LR_ERR_RANGE."""
+    p = wl.hgrn2_inputs(1, 64, 1, 128, seed=10)
+    p["g"] = torch.full_like(p["g"], 0.1)   # 64 steps of log2(0.1) = -212
+    q, k, v, g = (p[n].cuda() for n in ("q", "k", "v", "g"))
+    lr.hgrn2(q, k, v, g, H=1)
+    assert lr.lr_check_status(0) == lr.LR_ERR_RANGE
+    assert lr.lr_check_status(0) == 0
+
+
+def test_hgrn2_config4_full_size_sampled(lr):
+    """B=4, L=4096, hidden 2048 = 16 heads x 128, bf16, g = 0.2 + 0.8 sigmoid(f)."""
+    cfg = wl.CONFIGS[4]
+    p = wl.make_inputs(cfg, device="cuda")
+    o, Sf = lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=cfg.H)
+    torch.cuda.synchronize()
+    assert lr.lr_check_status(0) == 0
+    for b, h in ((0, 0), (3, 15), (1, 7)):
+        sl = slice(h * 128, (h + 1) * 128)
+        sub = {n: p[n][b:b + 1, :, sl].cpu() for n in ("q", "k", "v", "g")}
+        orf, Srf = oracle.hgrn2(sub["q"], sub["k"], sub["v"], sub["g"], 1)
+        assert rel_err(o[b:b + 1, :, sl].float().cpu(), orf) <= TOL
+        assert rel_err(Sf[b:b + 1, h:h + 1].cpu(), Srf) <= TOL
