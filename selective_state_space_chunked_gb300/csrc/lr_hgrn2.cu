@@ -14,17 +14,19 @@
 // Lambda): 2^(Lambda_t - Lambda_s) = 2^(Lambda_t - m) 2^(m - Lambda_s).  With
 // V~ = 2^(m - Lambda) (.) V and S~ = diag(2^m) S,
 //
-//   O   = 2^(Lambda - m) (.) ( tril(Q K^T) V~  +  Q S~^T )        (one accumulator)
+//   O   = 2^(Lambda - m) (.) ( tril(Q K^T) V~  +  2^m (.) Q S^T )
 //   dS^T = K^T (2^(Lambda_C - Lambda) (.) V)                       (state update, in TMEM)
 //
 // Four tcgen05 MMAs per chunk (bf16 operands in shared memory, fp32
 // accumulators in tensor memory):
 //   P   = Q K^T            M=64  N=64 K=128   A = Q (K-major),  B = K (K-major)
-//   O   = Q S~^T           M=64  N=32 K=128   B = S~ rows (K-major, written by the block)
+//   OX  = Q S^T            M=64  N=32 K=128   B = bf16 state rows (K-major, written by the block)
 //   dSt = K^T V~'          M=128 N=32 K=64    A = the same K tile read MN-major
-//   O  += tril(P) V~       M=64  N=32 K=64    A = masked P (bf16, written by the block)
-// Q, K (128B-swizzled) and the block's V, g columns arrive by TMA, two chunks
-// in flight.  Rows of S evolve independently (diag(g) scales rows), so a
+//   OI  = tril(P) V~       M=64  N=32 K=64    A = masked P (bf16, written by the block)
+// P and OX of chunk c+1 depend only on its Q, K and the state after chunk c,
+// so they are issued as soon as chunk c's state update is written and run
+// while the block computes chunk c+1's gates.  Q, K (128B-swizzled) and the
+// block's V, g columns arrive by TMA, two chunks in flight.  Rows of S evolve independently (diag(g) scales rows), so a
 // thread block owns 32 value rows of one (batch, head): 4 blocks per head.
 // The fp32 state lives in registers (thread j holds column j of its 32 rows)
 // and is updated elementwise from dS^T; it never leaves the chip between
@@ -60,7 +62,7 @@ constexpr uint32_t STAGE_BYTES = 2 * Q_BYTES + 2 * VG_BYTES;
 constexpr uint32_t OFF_P = STAGES * STAGE_BYTES;   // masked P, [64 t][64 s] swizzled
 constexpr uint32_t OFF_VT = OFF_P + 8192;          // V~ as [32 i][64 s] swizzled
 constexpr uint32_t OFF_VTP = OFF_VT + 4096;        // V~' as [32 i][64 s] swizzled
-constexpr uint32_t OFF_SB = OFF_VTP + 4096;        // S~ as [32 i][128 j], two swizzled halves
+constexpr uint32_t OFF_SB = OFF_VTP + 4096;        // bf16 state rows [32 i][128 j], two swizzled halves
 constexpr uint32_t OFF_LAM = OFF_SB + 8192;        // Lambda, float [64][32], 16-byte groups XOR-swizzled
 constexpr uint32_t OFF_TOT = OFF_LAM + 8192;       // per-warp partial sums, float [4][32]
 constexpr uint32_t OFF_L0 = OFF_TOT + 512;         // Lambda_0, float [32]
@@ -73,8 +75,8 @@ static_assert(OFF_P % 1024 == 0 && OFF_VT % 1024 == 0 && OFF_VTP % 1024 == 0 &&
                   OFF_SB % 1024 == 0 && STAGE_BYTES % 1024 == 0,
               "swizzled operand tiles must be 1024-byte aligned");
 
-constexpr uint32_t TMEM_COLS = 128;
-constexpr uint32_t T_P = 0, T_O = 64, T_S = 96;   // accumulator columns
+constexpr uint32_t TMEM_COLS = 256;  // two blocks per SM fill the 512 columns exactly
+constexpr uint32_t T_P = 0, T_OI = 64, T_OX = 96, T_S = 128;   // accumulator columns
 
 constexpr uint32_t IDESC_P = umma_idesc_bf16(64, 64, 0, 0);
 constexpr uint32_t IDESC_O = umma_idesc_bf16(64, RB, 0, 0);
@@ -149,15 +151,50 @@ __global__ void __launch_bounds__(hg::THREADS)
         tma_load_3d(stg + 2 * Q_BYTES, &tm_v, &full[st], vcol, c * C, b);
         tma_load_3d(stg + 2 * Q_BYTES + VG_BYTES, &tm_g, &full[st], vcol, c * C, b);
     };
+    // thread 0: P = Q K^T and OX = Q S^T for the chunk whose inputs sit in stage st
+    auto issue_p_ox = [&](int st) {
+        const uint32_t sQ = smem_u32(sm + st * STAGE_BYTES), sK = sQ + Q_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+            umma_bf16(tmem + T_P, umma_smem_desc(sQ + off, 16, 1024),
+                      umma_smem_desc(sK + off, 16, 1024), IDESC_P, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DK / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+            umma_bf16(tmem + T_OX, umma_smem_desc(sQ + off, 16, 1024),
+                      umma_smem_desc(smem_u32(SB) + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024),
+                      IDESC_O, kk > 0);
+        }
+        umma_commit(bar_p);
+    };
+    // bf16 copy of the state rows [i][j] (K-major B operand of Q S^T)
+    auto write_state_bf16 = [&]() {
+        const int j = tid, hj = j >> 6, jc = j & 63;
+#pragma unroll
+        for (int i = 0; i < RB; ++i)
+            *reinterpret_cast<__nv_bfloat16 *>(SB + hj * 4096 + sw128_offset(i, jc)) =
+                __float2bfloat16_rn(S[i]);
+    };
+
+    write_state_bf16();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
     if (tid == 0) {
         issue(0, 0);
         if (n_chunks > 1) issue(1, 1);
+        if (mbar_wait_bounded(&full[0], 0, timeout_ns)) {
+            tc_fence_after();
+            issue_p_ox(0);
+        }
     }
 
     for (int c = 0; c < n_chunks; ++c) {
         const int st = c & 1;
         unsigned char *stg = sm + st * STAGE_BYTES;
-        const uint32_t sQ = smem_u32(stg), sK = sQ + Q_BYTES;
+        const uint32_t sK = smem_u32(stg) + Q_BYTES;
         const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(stg + 2 * Q_BYTES);
         const __nv_bfloat16 *sG = sV + C * RB;
         const int t0 = c * C;
@@ -166,16 +203,6 @@ __global__ void __launch_bounds__(hg::THREADS)
         if (__syncthreads_or(!ok_in)) {
             if (tid == 0) hg_report(LR_ERR_TIMEOUT);
             break;
-        }
-        if (tid == 0) {  // P = Q K^T
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                umma_bf16(tmem + T_P, umma_smem_desc(sQ + off, 16, 1024),
-                          umma_smem_desc(sK + off, 16, 1024), IDESC_P, kk > 0);
-            }
-            umma_commit(bar_p);
         }
 
         // ---- cumulative log2 gates: warp w takes rows 16w..16w+15, lane = value channel
@@ -193,10 +220,39 @@ __global__ void __launch_bounds__(hg::THREADS)
             if (warp == 0) L0S[lane] = loc[0];
         }
         __syncthreads();
-        float m, lc;
+
+        // ---- causal mask of P = Q K^T (issued at the end of the previous chunk)
+        bool ok = mbar_wait_bounded(bar_p, c & 1, timeout_ns);
+        tc_fence_after();
         {
-            float off = 0.0f;
-            lc = 0.0f;
+            const uint32_t ta = tmem + T_P + (uint32_t(warp * 32) << 16);
+            const int t = 16 * warp + lane;  // valid for lane < 16 (M = 64 layout)
+            float pa[32], pb[32];
+            tmem_ld32_nowait(ta, pa);
+            tmem_ld32_nowait(ta + 32, pb);
+            tmem_ld_wait();
+            if (lane < 16) {
+#pragma unroll
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int s0 = chunk * 8 + 2 * e;
+                        const float v0 = s0 < 32 ? pa[s0] : pb[s0 - 32];
+                        const float v1 = s0 + 1 < 32 ? pa[s0 + 1] : pb[s0 + 1 - 32];
+                        __nv_bfloat162 pr = __floats2bfloat162_rn(s0 <= t ? v0 : 0.0f,
+                                                                  s0 + 1 <= t ? v1 : 0.0f);
+                        w4[e] = *reinterpret_cast<uint32_t *>(&pr);
+                    }
+                    *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+        }
+
+        // ---- Lambda, reference m, V~ and V~'
+        {
+            float off = 0.0f, lc = 0.0f;
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
                 const float tw = TOT[w * 32 + lane];
@@ -204,79 +260,35 @@ __global__ void __launch_bounds__(hg::THREADS)
                 lc += tw;
             }
             const float l0 = L0S[lane];
-            m = 0.5f * (l0 + lc);
+            const float m = 0.5f * (l0 + lc);
             if (warp == 0 && !(l0 - lc <= kMaxSpread)) hg_report(LR_ERR_RANGE);
+            uint32_t vt[8], vtp[8];  // bf16 pairs of this lane's row, columns 16w .. 16w+15
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 16; u += 2) {
                 const int t = 16 * warp + u;
-                const float lam = loc[u] + off;
-                LAM[lam_index(t, lane)] = lam;
-                const float v = __bfloat162float(sV[t * RB + lane]);
-                *reinterpret_cast<__nv_bfloat16 *>(VT + sw128_offset(lane, t)) =
-                    __float2bfloat16_rn(ex2_approx(m - lam) * v);
-                *reinterpret_cast<__nv_bfloat16 *>(VTP + sw128_offset(lane, t)) =
-                    __float2bfloat16_rn(ex2_approx(lc - lam) * v);
+                const float lam0 = loc[u] + off, lam1 = loc[u + 1] + off;
+                LAM[lam_index(t, lane)] = lam0;
+                LAM[lam_index(t + 1, lane)] = lam1;
+                const float v0 = __bfloat162float(sV[t * RB + lane]);
+                const float v1 = __bfloat162float(sV[(t + 1) * RB + lane]);
+                __nv_bfloat162 a = __floats2bfloat162_rn(ex2_approx(m - lam0) * v0,
+                                                         ex2_approx(m - lam1) * v1);
+                __nv_bfloat162 bq = __floats2bfloat162_rn(ex2_approx(lc - lam0) * v0,
+                                                          ex2_approx(lc - lam1) * v1);
+                vt[u / 2] = *reinterpret_cast<uint32_t *>(&a);
+                vtp[u / 2] = *reinterpret_cast<uint32_t *>(&bq);
+            }
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {   // two 16-byte chunks: columns 16w + 8*h8 ..
+                const uint32_t off8 = sw128_offset(lane, 16 * warp + 8 * h8);
+                *reinterpret_cast<uint4 *>(VT + off8) =
+                    make_uint4(vt[4 * h8], vt[4 * h8 + 1], vt[4 * h8 + 2], vt[4 * h8 + 3]);
+                *reinterpret_cast<uint4 *>(VTP + off8) =
+                    make_uint4(vtp[4 * h8], vtp[4 * h8 + 1], vtp[4 * h8 + 2], vtp[4 * h8 + 3]);
             }
             if (warp == 0) {
                 MS[lane] = m;
                 LCS[lane] = lc;
-            }
-        }
-        __syncthreads();
-        // ---- S~ = diag(2^m) S as bf16 rows [i][j] for the Q S~^T product
-        {
-            const int j = tid, hj = j >> 6, jc = j & 63;
-#pragma unroll
-            for (int i = 0; i < RB; ++i)
-                *reinterpret_cast<__nv_bfloat16 *>(SB + hj * 4096 + sw128_offset(i, jc)) =
-                    __float2bfloat16_rn(ex2_approx(MS[i]) * S[i]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            // O = Q S~^T
-#pragma unroll
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                umma_bf16(tmem + T_O, umma_smem_desc(sQ + off, 16, 1024),
-                          umma_smem_desc(smem_u32(SB) + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024),
-                          IDESC_O, kk > 0);
-            }
-            // dS^T = K^T V~'  (K tile read MN-major: 64-column halves 8 KB apart)
-#pragma unroll
-            for (int kk = 0; kk < C / 16; ++kk)
-                umma_bf16(tmem + T_S, umma_smem_desc(sK + kk * 2048, 8192, 1024),
-                          umma_smem_desc(smem_u32(VTP) + kk * 32, 16, 1024), IDESC_S, kk > 0);
-        }
-        // ---- causal mask of P = Q K^T into bf16 shared memory
-        bool ok = mbar_wait_bounded(bar_p, c & 1, timeout_ns);
-        tc_fence_after();
-        {
-            const uint32_t ta = tmem + T_P + (uint32_t(warp * 32) << 16);
-            const int t = 16 * warp + lane;  // valid for lane < 16 (M = 64 layout)
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) {
-                float pv[16];
-                tmem_ld16(ta + c0, pv);
-                if (lane < 16) {
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int s0 = c0 + 8 * q + 2 * e;
-                            const float a0 = s0 <= t ? pv[8 * q + 2 * e] : 0.0f;
-                            const float a1 = s0 + 1 <= t ? pv[8 * q + 2 * e + 1] : 0.0f;
-                            __nv_bfloat162 pr = __floats2bfloat162_rn(a0, a1);
-                            w4[e] = *reinterpret_cast<uint32_t *>(&pr);
-                        }
-                        const int chunk = (c0 >> 3) + q;
-                        *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) =
-                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                    }
-                }
             }
         }
         fence_proxy_async_smem();
@@ -285,22 +297,29 @@ __global__ void __launch_bounds__(hg::THREADS)
             if (tid == 0) hg_report(LR_ERR_TIMEOUT);
             break;
         }
-        if (tid == 0) {  // O += tril(P) V~
+        if (tid == 0) {
             tc_fence_after();
+            // dS^T = K^T V~'  (K tile read MN-major: 64-column halves 8 KB apart)
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
-                umma_bf16(tmem + T_O, umma_smem_desc(smem_u32(Ps) + kk * 32, 16, 1024),
-                          umma_smem_desc(smem_u32(VT) + kk * 32, 16, 1024), IDESC_O, 1);
+                umma_bf16(tmem + T_S, umma_smem_desc(sK + kk * 2048, 8192, 1024),
+                          umma_smem_desc(smem_u32(VTP) + kk * 32, 16, 1024), IDESC_S, kk > 0);
+            // OI = tril(P) V~
+#pragma unroll
+            for (int kk = 0; kk < C / 16; ++kk)
+                umma_bf16(tmem + T_OI, umma_smem_desc(smem_u32(Ps) + kk * 32, 16, 1024),
+                          umma_smem_desc(smem_u32(VT) + kk * 32, 16, 1024), IDESC_O, kk > 0);
             umma_commit(bar_o);
         }
         ok = mbar_wait_bounded(bar_o, c & 1, timeout_ns);
         tc_fence_after();
-        {   // ---- output rows: o_t = 2^(Lambda_t - m) O_t
-            const uint32_t ta = tmem + T_O + (uint32_t(warp * 32) << 16);
+        {   // ---- output rows: o_t = 2^(Lambda_t - m) (OI_t + 2^m OX_t)
+            const uint32_t lw = uint32_t(warp * 32) << 16;
             const int t = 16 * warp + lane;
-            float ov[32];
-            tmem_ld16(ta, *reinterpret_cast<float(*)[16]>(ov));
-            tmem_ld16(ta + 16, *reinterpret_cast<float(*)[16]>(ov + 16));
+            float oi[32], ox[32];
+            tmem_ld32_nowait(tmem + T_OI + lw, oi);
+            tmem_ld32_nowait(tmem + T_OX + lw, ox);
+            tmem_ld_wait();
             if (lane < 16 && t0 + t < L) {
                 uint4 w4[4];
                 uint32_t *wp = reinterpret_cast<uint32_t *>(w4);
@@ -308,10 +327,12 @@ __global__ void __launch_bounds__(hg::THREADS)
                 for (int i = 0; i < RB; i += 4) {
                     const float4 lm = *reinterpret_cast<const float4 *>(LAM + lam_index(t, i));
                     const float4 mm = *reinterpret_cast<const float4 *>(MS + i);
-                    __nv_bfloat162 p0 = __floats2bfloat162_rn(ov[i] * ex2_approx(lm.x - mm.x),
-                                                              ov[i + 1] * ex2_approx(lm.y - mm.y));
-                    __nv_bfloat162 p1 = __floats2bfloat162_rn(ov[i + 2] * ex2_approx(lm.z - mm.z),
-                                                              ov[i + 3] * ex2_approx(lm.w - mm.w));
+                    const float r0 = fmaf(ex2_approx(mm.x), ox[i], oi[i]) * ex2_approx(lm.x - mm.x);
+                    const float r1 = fmaf(ex2_approx(mm.y), ox[i + 1], oi[i + 1]) * ex2_approx(lm.y - mm.y);
+                    const float r2 = fmaf(ex2_approx(mm.z), ox[i + 2], oi[i + 2]) * ex2_approx(lm.z - mm.z);
+                    const float r3 = fmaf(ex2_approx(mm.w), ox[i + 3], oi[i + 3]) * ex2_approx(lm.w - mm.w);
+                    __nv_bfloat162 p0 = __floats2bfloat162_rn(r0, r1);
+                    __nv_bfloat162 p1 = __floats2bfloat162_rn(r2, r3);
                     wp[i / 2] = *reinterpret_cast<uint32_t *>(&p0);
                     wp[i / 2 + 1] = *reinterpret_cast<uint32_t *>(&p1);
                 }
@@ -320,20 +341,29 @@ __global__ void __launch_bounds__(hg::THREADS)
                 for (int q = 0; q < 4; ++q) dst[q] = w4[q];
             }
         }
-        {   // ---- state: S = diag(2^Lambda_C) S + dS
+        {   // ---- state: S = diag(2^Lambda_C) S + dS, and its bf16 copy for the next chunk
             const uint32_t ta = tmem + T_S + (uint32_t(warp * 32) << 16);
             float ds[32];
-            tmem_ld16(ta, *reinterpret_cast<float(*)[16]>(ds));
-            tmem_ld16(ta + 16, *reinterpret_cast<float(*)[16]>(ds + 16));
+            tmem_ld32_nowait(ta, ds);
+            tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < RB; ++i) S[i] = fmaf(ex2_approx(LCS[i]), S[i], ds[i]);
+            write_state_bf16();
         }
+        fence_proxy_async_smem();
         tc_fence_before();
         if (__syncthreads_or(!ok)) {
             if (tid == 0) hg_report(LR_ERR_TIMEOUT);
             break;
         }
-        if (tid == 0 && c + 2 < n_chunks) issue(c + 2, st);
+        if (tid == 0) {
+            if (c + 2 < n_chunks) issue(c + 2, st);
+            if (c + 1 < n_chunks &&
+                mbar_wait_bounded(&full[(c + 1) & 1], ((c + 1) >> 1) & 1, timeout_ns)) {
+                tc_fence_after();
+                issue_p_ox((c + 1) & 1);
+            }
+        }
     }
 
     if (S_final != nullptr) {
