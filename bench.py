@@ -71,8 +71,47 @@ def algorithmic(cfg: wl.Config) -> dict:
 STEP_CONFIGS = (2, 3, 4)
 
 
-def step_configs():
-    return [wl.CONFIGS[k] for k in STEP_CONFIGS]
+def step_configs(only=None, seq_len=None):
+    """The step's workloads; ``only`` keeps one form and ``seq_len`` shortens
+    the sequences (profiling cases: a launch of the same kernel on a smaller
+    input, never a benchmark number)."""
+    import dataclasses
+    cfgs = [wl.CONFIGS[k] for k in STEP_CONFIGS]
+    if only:
+        cfgs = [c for c in cfgs if c.form == only]
+    if seq_len:
+        cfgs = [dataclasses.replace(c, L=seq_len) for c in cfgs]
+    return cfgs
+
+
+# ALU roofline of the selective scan.  Every (token, channel, state) element
+# costs one exp2 on the MUFU pipe (the discretised decay) and four fp32 ops on
+# the FMA pipe (the decay argument, the input product, the state FMA, the
+# readout FMA).  At 128 fp32 lanes and 32 exp2 results per clock per SM the
+# two pipes cap the update at min(128/4, 32/1) = 32 elements per clock per SM;
+# with 152 SMs at the 2070 MHz maximum clock that is 10.07 T elements/s.
+ALU_SMS = 152
+ALU_MAX_MHZ = 2070
+ALU_ELEMS_PER_CLK_SM = 32
+
+
+def alu_peak_gelem() -> float:
+    return ALU_SMS * ALU_MAX_MHZ * 1e6 * ALU_ELEMS_PER_CLK_SM / 1e9
+
+
+def kernel_roofline(cfg: wl.Config, a: dict, ms: float, peaks: dict) -> dict:
+    """Roofline entry of one scan's kernel for one launch of ``ms``."""
+    sec = ms * 1e-3
+    if cfg.form == "selective":
+        ach = a["units"] * cfg.N / sec / 1e9
+        peak = alu_peak_gelem()
+        return {"kernel": cfg.name, "bound": "alu", "achieved": ach, "peak": peak,
+                "unit": "Gelem/s", "frac": ach / peak, "traffic": traffic_for(cfg),
+                "peak_source": "derived: 152 SMs x 2070 MHz x 32 state updates/clk/SM"}
+    ach = a["bytes"] / sec / 1e9
+    return {"kernel": cfg.name, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": traffic_for(cfg),
+            "peak_source": peaks["source"]}
 
 
 # ----------------------------------------------------------------------------
@@ -238,7 +277,7 @@ def gpu_arm(args):
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
     from selective_state_space_chunked_gb300 import binding as lr
-    cfgs = step_configs()
+    cfgs = step_configs(args.only, args.seq_len)
     inputs = [wl.make_inputs(c, device=dev) for c in cfgs]
     calls = [make_call(lr, c, p) for c, p in zip(cfgs, inputs)]
     alg = [algorithmic(c) for c in cfgs]
@@ -311,14 +350,12 @@ def gpu_arm(args):
     value = world * units_step * args.steps / (total_ms * 1e-3)
     peaks = load_peaks()
     dom = max(range(len(cfgs)), key=lambda j: per_scan[j]["ms"])
-    roof = {"kernel": cfgs[dom].name, "bound": "hbm", "achieved": per_scan[dom]["gb_per_s"],
-            "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": per_scan[dom]["gb_per_s"] / peaks["hbm_gbs"],
-            "traffic": traffic_for(cfgs[dom].name), "peak_source": peaks["source"]}
+    rooflines = [kernel_roofline(c, a, d["ms"], peaks) for c, a, d in zip(cfgs, alg, per_scan)]
+    roof = dict(rooflines[dom])
     for d in per_scan:
         d["hbm_frac"] = d["gb_per_s"] / peaks["hbm_gbs"]
         if "tflop_per_s" in d:
-            d["tensor_frac"] = d["tflop_per_s"] / peaks["bf16_tflops"]
+            d["tensor_frac"] = d["tflop_per_s"] / peaks["bf16_tflops_sustained"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -330,6 +367,7 @@ def gpu_arm(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "per_scan": per_scan,
         "roofline": roof,
+        "rooflines": rooflines,
         "e2e": {"value": world * units_step / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": len(cfgs) * args.steps,
@@ -356,32 +394,38 @@ def load_peaks() -> dict:
                 "source": "fallback"}
 
 
-def kernel_source_digest() -> str:
-    """Digest of the library's CUDA sources: a stored ncu traffic figure is
-    used only while the kernels it was taken from are unchanged."""
-    import glob
+# CUDA sources each scan's kernel is compiled from.
+KERNEL_SOURCES = {"rglru": ("lr_diag_scan.cu", "lr_device.cuh"),
+                  "selective": ("lr_diag_scan.cu", "lr_device.cuh"),
+                  "hgrn2": ("lr_hgrn2.cu", "lr_device.cuh")}
+
+
+def kernel_source_digest(form: str) -> str:
+    """Digest of the sources of one scan's kernel: a stored ncu traffic figure
+    is used only while the kernel it was taken from is unchanged."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_chunked_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
-        with open(f, "rb") as fh:
+    for f in KERNEL_SOURCES[form]:
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def traffic_for(name: str):
+def traffic_for(cfg: wl.Config):
     """DRAM read+write bytes per full-size launch from the committed ncu
     summary (profiles/traffic.json), or None when it is missing or was taken
-    from kernels that have changed since."""
+    from a kernel that has changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_digest") != kernel_source_digest():
+    e = d.get(cfg.form)
+    if not e or e.get("source_digest") != kernel_source_digest(cfg.form) or e.get("L") != cfg.L:
         return None
-    return d.get("per_launch_bytes", {}).get(name)
+    return e.get("per_launch_bytes")
 
 
 # ----------------------------------------------------------------------------
@@ -391,7 +435,7 @@ def reference_arm(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    cfgs = step_configs()
+    cfgs = step_configs(args.only, args.seq_len)
     samples = [(cfg, *oracle_sample(cfg)) for cfg in cfgs]
     cb = None
     vals = []
@@ -424,6 +468,10 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the CPU oracle beside the GPU arm")
+    ap.add_argument("--only", choices=["rglru", "selective", "hgrn2"], default=None,
+                    help="run one scan of the step (profiling case)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="shorter sequences for a profiling case (not a benchmark number)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

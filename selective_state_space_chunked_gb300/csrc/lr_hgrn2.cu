@@ -63,11 +63,11 @@ constexpr uint32_t OFF_P = STAGES * STAGE_BYTES;   // masked P, [64 t][64 s] swi
 constexpr uint32_t OFF_VT = OFF_P + 8192;          // V~ as [32 i][64 s] swizzled
 constexpr uint32_t OFF_VTP = OFF_VT + 4096;        // V~' as [32 i][64 s] swizzled
 constexpr uint32_t OFF_SB = OFF_VTP + 4096;        // bf16 state rows [32 i][128 j], two swizzled halves
-constexpr uint32_t OFF_LAM = OFF_SB + 8192;        // Lambda, float [64][32], 16-byte groups XOR-swizzled
+constexpr uint32_t OFF_LAM = OFF_SB + 8192;        // 2^(Lambda - m), float [64][32], 16-byte groups XOR-swizzled
 constexpr uint32_t OFF_TOT = OFF_LAM + 8192;       // per-warp partial sums, float [4][32]
 constexpr uint32_t OFF_L0 = OFF_TOT + 512;         // Lambda_0, float [32]
 constexpr uint32_t OFF_M = OFF_L0 + 128;           // m, float [32]
-constexpr uint32_t OFF_LC = OFF_M + 128;           // Lambda_C, float [32]
+constexpr uint32_t OFF_LC = OFF_M + 128;           // 2^Lambda_C, float [32]
 constexpr uint32_t OFF_BAR = OFF_LC + 128;         // full[2], bar_p, bar_o
 constexpr uint32_t OFF_TMEM = OFF_BAR + 32;
 constexpr uint32_t SMEM = OFF_TMEM + 16;
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(hg::THREADS)
     uint64_t *bar_p = full + 2;
     uint64_t *bar_o = full + 3;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
-    float *LAM = reinterpret_cast<float *>(sm + OFF_LAM);
+    float *LAM = reinterpret_cast<float *>(sm + OFF_LAM);  // 2^(Lambda - m) per [t][i]
     float *TOT = reinterpret_cast<float *>(sm + OFF_TOT);
     float *L0S = reinterpret_cast<float *>(sm + OFF_L0);
     float *MS = reinterpret_cast<float *>(sm + OFF_M);
@@ -262,19 +262,21 @@ __global__ void __launch_bounds__(hg::THREADS)
             const float l0 = L0S[lane];
             const float m = 0.5f * (l0 + lc);
             if (warp == 0 && !(l0 - lc <= kMaxSpread)) hg_report(LR_ERR_RANGE);
+            // 2^(Lambda_C - Lambda) = 2^(m - Lambda) 2^(Lambda_C - m); both factors stay
+            // inside fp32 range because |Lambda - m| and |Lambda_C - m| are at most 80
+            const float cm = ex2_approx(lc - m);
             uint32_t vt[8], vtp[8];  // bf16 pairs of this lane's row, columns 16w .. 16w+15
 #pragma unroll
             for (int u = 0; u < 16; u += 2) {
                 const int t = 16 * warp + u;
                 const float lam0 = loc[u] + off, lam1 = loc[u + 1] + off;
-                LAM[lam_index(t, lane)] = lam0;
-                LAM[lam_index(t + 1, lane)] = lam1;
+                LAM[lam_index(t, lane)] = ex2_approx(lam0 - m);
+                LAM[lam_index(t + 1, lane)] = ex2_approx(lam1 - m);
                 const float v0 = __bfloat162float(sV[t * RB + lane]);
                 const float v1 = __bfloat162float(sV[(t + 1) * RB + lane]);
-                __nv_bfloat162 a = __floats2bfloat162_rn(ex2_approx(m - lam0) * v0,
-                                                         ex2_approx(m - lam1) * v1);
-                __nv_bfloat162 bq = __floats2bfloat162_rn(ex2_approx(lc - lam0) * v0,
-                                                          ex2_approx(lc - lam1) * v1);
+                const float w0 = ex2_approx(m - lam0) * v0, w1 = ex2_approx(m - lam1) * v1;
+                __nv_bfloat162 a = __floats2bfloat162_rn(w0, w1);
+                __nv_bfloat162 bq = __floats2bfloat162_rn(w0 * cm, w1 * cm);
                 vt[u / 2] = *reinterpret_cast<uint32_t *>(&a);
                 vtp[u / 2] = *reinterpret_cast<uint32_t *>(&bq);
             }
@@ -287,8 +289,8 @@ __global__ void __launch_bounds__(hg::THREADS)
                     make_uint4(vtp[4 * h8], vtp[4 * h8 + 1], vtp[4 * h8 + 2], vtp[4 * h8 + 3]);
             }
             if (warp == 0) {
-                MS[lane] = m;
-                LCS[lane] = lc;
+                MS[lane] = ex2_approx(m);
+                LCS[lane] = ex2_approx(lc);
             }
         }
         fence_proxy_async_smem();
@@ -325,12 +327,12 @@ __global__ void __launch_bounds__(hg::THREADS)
                 uint32_t *wp = reinterpret_cast<uint32_t *>(w4);
 #pragma unroll
                 for (int i = 0; i < RB; i += 4) {
-                    const float4 lm = *reinterpret_cast<const float4 *>(LAM + lam_index(t, i));
-                    const float4 mm = *reinterpret_cast<const float4 *>(MS + i);
-                    const float r0 = fmaf(ex2_approx(mm.x), ox[i], oi[i]) * ex2_approx(lm.x - mm.x);
-                    const float r1 = fmaf(ex2_approx(mm.y), ox[i + 1], oi[i + 1]) * ex2_approx(lm.y - mm.y);
-                    const float r2 = fmaf(ex2_approx(mm.z), ox[i + 2], oi[i + 2]) * ex2_approx(lm.z - mm.z);
-                    const float r3 = fmaf(ex2_approx(mm.w), ox[i + 3], oi[i + 3]) * ex2_approx(lm.w - mm.w);
+                    const float4 e1 = *reinterpret_cast<const float4 *>(LAM + lam_index(t, i));
+                    const float4 em = *reinterpret_cast<const float4 *>(MS + i);
+                    const float r0 = fmaf(em.x, ox[i], oi[i]) * e1.x;
+                    const float r1 = fmaf(em.y, ox[i + 1], oi[i + 1]) * e1.y;
+                    const float r2 = fmaf(em.z, ox[i + 2], oi[i + 2]) * e1.z;
+                    const float r3 = fmaf(em.w, ox[i + 3], oi[i + 3]) * e1.w;
                     __nv_bfloat162 p0 = __floats2bfloat162_rn(r0, r1);
                     __nv_bfloat162 p1 = __floats2bfloat162_rn(r2, r3);
                     wp[i / 2] = *reinterpret_cast<uint32_t *>(&p0);
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(hg::THREADS)
             tmem_ld32_nowait(ta, ds);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < RB; ++i) S[i] = fmaf(ex2_approx(LCS[i]), S[i], ds[i]);
+            for (int i = 0; i < RB; ++i) S[i] = fmaf(LCS[i], S[i], ds[i]);
             write_state_bf16();
         }
         fence_proxy_async_smem();
