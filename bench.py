@@ -185,6 +185,12 @@ def barrier(world: int):
         torch.distributed.barrier()
 
 
+def job_throughput(world: int, units_per_rank_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's
+    time (each rank runs the same per-rank workload: weak scaling)."""
+    return world * units_per_rank_step * steps / (max_ms * 1e-3)
+
+
 def max_over_ranks(v: float, world: int, device) -> float:
     if world == 1:
         return v
@@ -347,7 +353,7 @@ def gpu_arm(args):
     del host_inputs, host_calls
 
     units_step = sum(a["units"] for a in alg)
-    value = world * units_step * args.steps / (total_ms * 1e-3)
+    value = job_throughput(world, units_step, args.steps, total_ms)
     peaks = load_peaks()
     dom = max(range(len(cfgs)), key=lambda j: per_scan[j]["ms"])
     rooflines = [kernel_roofline(c, a, d["ms"], peaks) for c, a, d in zip(cfgs, alg, per_scan)]
