@@ -354,24 +354,31 @@ __global__ void __launch_bounds__(RgCfg<IO>::THREADS)
 // Selective SSM
 // ============================================================================
 // Warp roles in a block of DC channels:
-//   compute warps: a lane pair per channel, 8 states per lane.  In batches of
-//     8 steps each lane computes delta = softplus(dt) and u = delta x for 4
-//     of the steps and swaps them with its partner; both lanes advance their
-//     8 states through the 8 steps (h[n] = exp(delta A[n]) h[n] + u B_t[n],
-//     partial C_t . h); the pair adds its halves with 4 shuffles; each lane
-//     finishes y = (C.h + D x) silu(z) for its 4 steps and stores it.
+//   compute warps: LPC lanes per channel, N / LPC states per lane.  In
+//     batches of 8 steps each lane computes delta = softplus(dt) and
+//     u = delta x for 8 / LPC of the steps and the channel's lanes share them
+//     by shuffles; every lane advances its states through the 8 steps
+//     (h[n] = exp(delta A[n]) h[n] + u B_t[n], partial C_t . h); a butterfly
+//     over the channel's lanes sums the partials so that each lane ends up
+//     with the full C_t . h of its own steps, finishes
+//     y = (C.h + D x) silu(z) for them and stores it.  LPC = 2 (8 states per
+//     lane) is the measured optimum on GB300: 4 lanes double the resident
+//     warps but cost more shuffles and fewer independent chains per lane and
+//     ran 1.5x slower; 1 lane per channel leaves too few warps per SM.
 //   producer warp: keeps STAGES tiles of x, dt, z, B_t, C_t in flight by TMA
 //     and widens each tile's B_t, C_t rows (shared by all channels) to fp32
 //     once, so the compute lanes read them with broadcast 16-byte loads.
-template <typename IO, int DC_>
+template <typename IO, int DC_, int LPC_>
 struct SelCfg {
     static constexpr int DC = DC_;                       // channels per block
-    static constexpr int CWARPS = DC / 16;               // 16 channels per compute warp
+    static constexpr int LPC = LPC_;                     // lanes per channel
+    static constexpr int CWARPS = DC * LPC / 32;
     static constexpr int THREADS = 32 * (CWARPS + 1);    // + producer warp
-    static constexpr int N = 16, NH = 8;
+    static constexpr int N = 16, NS = N / LPC, NP = NS / 2;
     static constexpr int T = 32;
     static constexpr int STAGES = 4;
     static constexpr int BATCH = 8;
+    static constexpr int OWN = BATCH / LPC;              // steps a lane prepares per batch
     static constexpr int TILE = T * DC;                  // x / dt / z tile elements
     static constexpr int TILE_N = T * N;                 // B / C tile elements
     static constexpr int STAGE_ELEMS = 3 * TILE + 2 * TILE_N;
@@ -380,89 +387,90 @@ struct SelCfg {
     static constexpr size_t OFF_BAR = OFF_BC + size_t(STAGES) * T * 2 * N * 4;
     static constexpr size_t SMEM = OFF_BAR + 3 * STAGES * 8 + 16;
     static constexpr int kAgg = 1 + N, kIncl = N;
-    static_assert(T % BATCH == 0 && DC % 16 == 0, "tile shape");
+    static_assert(T % BATCH == 0 && (DC * LPC) % 32 == 0 && (LPC == 2 || LPC == 4), "tile shape");
 };
 
-// Advances 8 states by one step: h = exp(delta A) h + u B, and returns
-// sum_n C[n] h[n] over these states (when READOUT).
-template <bool READOUT>
-__device__ __forceinline__ float sel_step8(float2 (&h)[4], const float2 (&A2)[4], float dl, float u,
-                                           const float *Bp, const float *Cp) {
-    const float2 dd = make_float2(dl, dl);
-    const float2 uu = make_float2(u, u);
-    const float4 b0 = *reinterpret_cast<const float4 *>(Bp);
-    const float4 b1 = *reinterpret_cast<const float4 *>(Bp + 4);
-    const float2 Bv[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
-                          make_float2(b1.z, b1.w)};
-    float2 Cv[4];
-    if (READOUT) {
-        const float4 c0 = *reinterpret_cast<const float4 *>(Cp);
-        const float4 c1 = *reinterpret_cast<const float4 *>(Cp + 4);
-        Cv[0] = make_float2(c0.x, c0.y);
-        Cv[1] = make_float2(c0.z, c0.w);
-        Cv[2] = make_float2(c1.x, c1.y);
-        Cv[3] = make_float2(c1.z, c1.w);
-    }
-    float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 arg = __fmul2_rn(dd, A2[q]);
-        const float2 a = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
-        h[q] = __ffma2_rn(a, h[q], __fmul2_rn(uu, Bv[q]));
-        if (READOUT) acc = __ffma2_rn(Cv[q], h[q], acc);
-    }
-    return acc.x + acc.y;
-}
-
-// One T-step tile of one lane's 8 states.  `rows` = steps of the tile inside
+// One T-step tile of one lane's states.  `rows` = steps of the tile inside
 // the sequence (and 0 for a channel past D in the ragged mode).  MODE is
-// warp-uniform, so the lane-pair shuffles always run converged.
-template <typename IO, int DC, bool ACC, bool HAS_Z, bool SOFTPLUS, int MODE>
+// warp-uniform, so the shuffles always run converged.  Lane r of a channel's
+// group (r = lane % LPC) prepares steps j0 + r + LPC m of each batch and
+// finishes the outputs of the same steps.  Inside a batch the lane walks its
+// states in groups of four (one 16-byte B_t and C_t load per step and group)
+// and, per group, all 8 steps: the group's decays for the 8 steps are
+// independent of each other and of the state, so they issue ahead of the
+// serial h chain.
+template <typename IO, int DC, int LPC, bool ACC, bool HAS_Z, bool SOFTPLUS, int MODE>
 __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *zs, const float *bc,
-                                         const float2 (&A2)[4], float2 (&h)[4], float &dsum,
-                                         float dsk, IO *yp, int D, int rows, int half) {
-    using C = SelCfg<IO, DC>;
+                                         const float2 (&A2)[SelCfg<IO, DC, LPC>::NP],
+                                         float2 (&h)[SelCfg<IO, DC, LPC>::NP], float &dsum,
+                                         float dsk, IO *yp, int D, int rows, int r, int lane) {
+    using C = SelCfg<IO, DC, LPC>;
+    constexpr int OWN = C::OWN;
     const unsigned FULL = 0xffffffffu;
+    const int g0 = lane & ~(LPC - 1);   // first lane of this channel's group
 #pragma unroll 1
     for (int j0 = 0; j0 < C::T; j0 += C::BATCH) {
-        // this lane owns steps j0 + half + 2m, m = 0..3
-        float xv[4], dl[4], u[4], dlo[4], uo[4];
+        float xv[OWN], dl[OWN], u[OWN];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int j = j0 + half + 2 * m;
+        for (int m = 0; m < OWN; ++m) {
+            const int j = j0 + r + LPC * m;
             xv[m] = Io<IO>::to_f(xs[j * DC]);
             const float dtv = Io<IO>::to_f(dts[j * DC]);
             dl[m] = SOFTPLUS ? softplus_t<ACC>(dtv) : dtv;
             if (MODE != kFull) dl[m] = j < rows ? dl[m] : 0.0f;  // rows past L: identity steps
             u[m] = dl[m] * xv[m];
         }
+        float dqs[C::BATCH], uqs[C::BATCH];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            dlo[m] = __shfl_xor_sync(FULL, dl[m], 1);
-            uo[m] = __shfl_xor_sync(FULL, u[m], 1);
+        for (int q = 0; q < C::BATCH; ++q) {
+            dqs[q] = __shfl_sync(FULL, dl[q / LPC], g0 | (q % LPC));
+            uqs[q] = __shfl_sync(FULL, u[q / LPC], g0 | (q % LPC));
+            if (MODE == kAggregate) dsum += dqs[q];
+        }
+        float2 ya[C::BATCH];
+#pragma unroll
+        for (int q = 0; q < C::BATCH; ++q) ya[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int g = 0; g < C::NP / 2; ++g) {
+#pragma unroll
+            for (int q = 0; q < C::BATCH; ++q) {
+                const float *row = bc + (j0 + q) * 2 * C::N + 4 * g;
+                const float2 dd = make_float2(dqs[q], dqs[q]);
+                const float2 uu = make_float2(uqs[q], uqs[q]);
+                const float4 b4 = *reinterpret_cast<const float4 *>(row);
+                const float2 a0 = __fmul2_rn(dd, A2[2 * g]), a1 = __fmul2_rn(dd, A2[2 * g + 1]);
+                const float2 e0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
+                const float2 e1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
+                h[2 * g] = __ffma2_rn(e0, h[2 * g], __fmul2_rn(uu, make_float2(b4.x, b4.y)));
+                h[2 * g + 1] = __ffma2_rn(e1, h[2 * g + 1], __fmul2_rn(uu, make_float2(b4.z, b4.w)));
+                if (MODE != kAggregate) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(row + C::N);
+                    ya[q] = __ffma2_rn(make_float2(c4.x, c4.y), h[2 * g], ya[q]);
+                    ya[q] = __ffma2_rn(make_float2(c4.z, c4.w), h[2 * g + 1], ya[q]);
+                }
+            }
         }
         float yq[C::BATCH];
 #pragma unroll
-        for (int q = 0; q < C::BATCH; ++q) {
-            const bool own = (q & 1) == half;
-            const float dq = own ? dl[q >> 1] : dlo[q >> 1];
-            const float uq = own ? u[q >> 1] : uo[q >> 1];
-            const float *row = bc + (j0 + q) * 2 * C::N;
-            if (MODE == kAggregate) {
-                sel_step8<false>(h, A2, dq, uq, row, row + C::N);
-                dsum += dq;
-            } else {
-                yq[q] = sel_step8<true>(h, A2, dq, uq, row, row + C::N);
-            }
-        }
+        for (int q = 0; q < C::BATCH; ++q) yq[q] = ya[q].x + ya[q].y;
         if (MODE != kAggregate) {
-            // lane pair reduction: this lane keeps its own steps
+            // butterfly over the group: at the level of bit b a lane keeps the
+            // steps whose bit b matches its own and adds its partner's share
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float mine = half ? yq[2 * m + 1] : yq[2 * m];
-                const float other = __shfl_xor_sync(FULL, half ? yq[2 * m] : yq[2 * m + 1], 1);
-                const int j = j0 + half + 2 * m;
-                float o = fmaf(dsk, xv[m], mine + other);
+            for (int bb = LPC / 2; bb >= 1; bb >>= 1) {
+                const bool hi = (r & bb) != 0;
+#pragma unroll
+                for (int q = 0; q < C::BATCH; ++q) {
+                    if ((q & (LPC - 1) & ~(2 * bb - 1)) != 0 || (q & bb) != 0) continue;
+                    const float send = hi ? yq[q] : yq[q | bb];
+                    const float keep = hi ? yq[q | bb] : yq[q];
+                    yq[q] = keep + __shfl_xor_sync(FULL, send, bb);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < OWN; ++m) {
+                const int j = j0 + r + LPC * m;
+                float o = fmaf(dsk, xv[m], yq[LPC * m]);
                 if (HAS_Z) o *= silu_f(Io<IO>::to_f(zs[j * DC]));
                 if (MODE == kFull || j < rows) __stcs(yp + size_t(j) * D, Io<IO>::from_f(o));
             }
@@ -470,8 +478,11 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
     }
 }
 
-template <typename IO, int DC, bool ACC, bool HAS_Z, bool SOFTPLUS>
-__global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
+// The minimum of one resident block lets ptxas keep the batch's decays and
+// partial sums in registers (~130) instead of serialising the update to fit a
+// smaller budget; shared memory, not registers, bounds the blocks per SM.
+template <typename IO, int DC, int LPC, bool ACC, bool HAS_Z, bool SOFTPLUS>
+__global__ void __launch_bounds__(SelCfg<IO, DC, LPC>::THREADS, 1)
     selective_scan_kernel(const __grid_constant__ CUtensorMap tm_x,
                           const __grid_constant__ CUtensorMap tm_dt,
                           const __grid_constant__ CUtensorMap tm_z,
@@ -481,7 +492,7 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
                           IO *__restrict__ y, float *__restrict__ h_final, int L, int D, int n_db,
                           int S, int tps, int n_tiles, LookbackWs ws, int withheld,
                           uint64_t timeout_ns) {
-    using C = SelCfg<IO, DC>;
+    using C = SelCfg<IO, DC, LPC>;
     constexpr bool has_z = HAS_Z;
     extern __shared__ __align__(128) unsigned char smem[];
     IO *tiles = reinterpret_cast<IO *>(smem);
@@ -570,14 +581,14 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
     }
 
     // ------------------------------------------------------------ compute warps
-    const int ch = tid >> 1;    // channel within the block
-    const int half = tid & 1;   // states [8 half, 8 half + 8)
+    const int ch = tid / LPC;   // channel within the block
+    const int r = tid % LPC;    // states [NS r, NS r + NS)
     const int d = d0 + ch;
     const bool vd = d < D;
-    float2 A2[4], h[4];         // A2 = A log2(e) = -exp(A_log) log2(e)
+    float2 A2[C::NP], h[C::NP]; // A2 = A log2(e) = -exp(A_log) log2(e)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int n = half * C::NH + 2 * q;
+    for (int q = 0; q < C::NP; ++q) {
+        const int n = r * C::NS + 2 * q;
         A2[q] = vd ? make_float2(-expf(A_log[size_t(d) * C::N + n]) * kLog2e,
                                  -expf(A_log[size_t(d) * C::N + n + 1]) * kLog2e)
                    : make_float2(0.0f, 0.0f);
@@ -598,29 +609,29 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
         const IO *xs = base + ch;
         const IO *dts = base + C::TILE + ch;
         const IO *zs = base + 2 * C::TILE + ch;
-        const float *bc = BCf + size_t(st) * C::T * 2 * C::N + half * C::NH;
+        const float *bc = BCf + size_t(st) * C::T * 2 * C::N + r * C::NS;
         IO *yp = y + (size_t(b) * L + t0) * D + d;
         (void)FULL;
-        const bool full_tile = t0 + C::T <= L && d0 + 16 * (warp + 1) <= D;
+        const bool full_tile = t0 + C::T <= L && d0 + (32 / LPC) * (warp + 1) <= D;
         if (agg_pass)
-            sel_tile<IO, DC, ACC, HAS_Z, SOFTPLUS, kAggregate>(xs, dts, zs, bc, A2, h, dsum, dsk, yp,
-                                                                D, L - t0, half);
+            sel_tile<IO, DC, LPC, ACC, HAS_Z, SOFTPLUS, kAggregate>(xs, dts, zs, bc, A2, h, dsum, dsk,
+                                                                     yp, D, L - t0, r, lane);
         else if (full_tile)
-            sel_tile<IO, DC, ACC, HAS_Z, SOFTPLUS, kFull>(xs, dts, zs, bc, A2, h, dsum, dsk, yp, D,
-                                                           C::T, half);
+            sel_tile<IO, DC, LPC, ACC, HAS_Z, SOFTPLUS, kFull>(xs, dts, zs, bc, A2, h, dsum, dsk, yp,
+                                                                D, C::T, r, lane);
         else
-            sel_tile<IO, DC, ACC, HAS_Z, SOFTPLUS, kRagged>(xs, dts, zs, bc, A2, h, dsum, dsk, yp,
-                                                             D, vd ? L - t0 : 0, half);
+            sel_tile<IO, DC, LPC, ACC, HAS_Z, SOFTPLUS, kRagged>(xs, dts, zs, bc, A2, h, dsum, dsk,
+                                                                  yp, D, vd ? L - t0 : 0, r, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
 
         if (agg_pass && v == ntl - 1) {
             constexpr int NC = 32 * C::CWARPS;
             const size_t slot = size_t(cb) * S + s;
-            float2 carry[4];
+            float2 carry[C::NP];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = half * C::NH + 2 * q;
+            for (int q = 0; q < C::NP; ++q) {
+                const int n = r * C::NS + 2 * q;
                 carry[q] = (vd && h0 != nullptr)
                                ? make_float2(h0[(size_t(b) * D + d) * C::N + n],
                                              h0[(size_t(b) * D + d) * C::N + n + 1])
@@ -628,10 +639,10 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
             }
             if (s > 0) {
                 float *ag = ws.agg + slot * C::kAgg * DC;
-                if (half == 0) ag[ch] = dsum;
+                if (r == 0) ag[ch] = dsum;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int n = half * C::NH + 2 * q;
+                for (int q = 0; q < C::NP; ++q) {
+                    const int n = r * C::NS + 2 * q;
                     ag[(1 + n) * DC + ch] = h[q].x;
                     ag[(2 + n) * DC + ch] = h[q].y;
                 }
@@ -639,9 +650,9 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
                 named_bar_sync(1, NC);
                 if (tid == 0 && s != withheld) st_release_gpu(&ws.flags[slot], kFlagAggregate);
                 float acc_d = 0.0f;  // composition of splits sp+1 .. s-1
-                float2 acc_h[4];
+                float2 acc_h[C::NP];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) acc_h[q] = make_float2(0.0f, 0.0f);
+                for (int q = 0; q < C::NP; ++q) acc_h[q] = make_float2(0.0f, 0.0f);
                 bool done = false;
                 for (int sp = s - 1; sp >= 0 && !done; --sp) {
                     const size_t sl = size_t(cb) * S + sp;
@@ -652,8 +663,8 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
                     if (fv == static_cast<int>(kFlagInclusive)) {
                         const float *in = ws.incl + sl * C::kIncl * DC;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int n = half * C::NH + 2 * q;
+                        for (int q = 0; q < C::NP; ++q) {
+                            const int n = r * C::NS + 2 * q;
                             const float px = pow2_t<ACC>(A2[q].x * acc_d);
                             const float py = pow2_t<ACC>(A2[q].y * acc_d);
                             carry[q].x = fmaf(px, __ldcg(&in[n * DC + ch]), acc_h[q].x);
@@ -663,8 +674,8 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
                     } else if (fv == static_cast<int>(kFlagAggregate)) {
                         const float *ax = ws.agg + sl * C::kAgg * DC;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int n = half * C::NH + 2 * q;
+                        for (int q = 0; q < C::NP; ++q) {
+                            const int n = r * C::NS + 2 * q;
                             const float px = pow2_t<ACC>(A2[q].x * acc_d);
                             const float py = pow2_t<ACC>(A2[q].y * acc_d);
                             acc_h[q].x = fmaf(px, __ldcg(&ax[(1 + n) * DC + ch]), acc_h[q].x);
@@ -674,15 +685,15 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
                     } else {
                         if (tid == 0) report_status(LR_ERR_TIMEOUT);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) carry[q] = acc_h[q];
+                        for (int q = 0; q < C::NP; ++q) carry[q] = acc_h[q];
                         done = true;
                     }
                 }
             }
             float *in = ws.incl + slot * C::kIncl * DC;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = half * C::NH + 2 * q;
+            for (int q = 0; q < C::NP; ++q) {
+                const int n = r * C::NS + 2 * q;
                 in[n * DC + ch] = fmaf(pow2_t<ACC>(A2[q].x * dsum), carry[q].x, h[q].x);
                 in[(n + 1) * DC + ch] = fmaf(pow2_t<ACC>(A2[q].y * dsum), carry[q].y, h[q].y);
                 h[q] = carry[q];
@@ -694,8 +705,8 @@ __global__ void __launch_bounds__(SelCfg<IO, DC>::THREADS)
     }
     if (h_final != nullptr && vd && s == S - 1) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int n = half * C::NH + 2 * q;
+        for (int q = 0; q < C::NP; ++q) {
+            const int n = r * C::NS + 2 * q;
             h_final[(size_t(b) * D + d) * C::N + n] = h[q].x;
             h_final[(size_t(b) * D + d) * C::N + n + 1] = h[q].y;
         }
@@ -812,6 +823,7 @@ uint64_t timeout_ns() {
 }
 
 constexpr int kSelDC = 32;
+constexpr int kSelLPC = 2;   // lanes per channel
 
 int current_device(int *dev) {
     if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return LR_ERR_CUDA;
@@ -889,8 +901,8 @@ int rglru_launch(const void *x, const void *r, const void *i, const float *a_log
 // ------------------------------------------------------------- selective host
 template <typename IO, bool ACC, bool HZ, bool SP>
 static int selective_resident(int dev) {
-    using C = SelCfg<IO, kSelDC>;
-    return kernel_blocks_per_sm<selective_scan_kernel<IO, kSelDC, ACC, HZ, SP>>(C::THREADS, C::SMEM,
+    using C = SelCfg<IO, kSelDC, kSelLPC>;
+    return kernel_blocks_per_sm<selective_scan_kernel<IO, kSelDC, kSelLPC, ACC, HZ, SP>>(C::THREADS, C::SMEM,
                                                                                dev);
 }
 
@@ -910,13 +922,13 @@ int selective_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p) {
     if (device_sm_count(&sms) != LR_OK || current_device(&dev) != LR_OK) return LR_ERR_CUDA;
     *p = DiagPlan{};
     p->dc = kSelDC;
-    p->tile_t = SelCfg<float, kSelDC>::T;
+    p->tile_t = SelCfg<float, kSelDC, kSelLPC>::T;
     p->n_cb = B * ((D + p->dc - 1) / p->dc);
     p->n_tiles = static_cast<int>((L + p->tile_t - 1) / p->tile_t);
     const int per_sm = io == LR_BF16 ? selective_resident_any<__nv_bfloat16, false>(dev, true, true)
                                      : selective_resident_any<float, true>(dev, true, true);
     if (per_sm <= 0) return LR_ERR_CUDA;
-    choose_splits(p, sms, per_sm, SelCfg<float, kSelDC>::kAgg, SelCfg<float, kSelDC>::kIncl);
+    choose_splits(p, sms, per_sm, SelCfg<float, kSelDC, kSelLPC>::kAgg, SelCfg<float, kSelDC, kSelLPC>::kIncl);
     return LR_OK;
 }
 
@@ -926,10 +938,10 @@ static int selective_launch_v(const CUtensorMap &mx, const CUtensorMap &mdt, con
                               const float *Dskip, const float *h0, void *y, float *h_final,
                               int64_t L, int64_t D, const DiagPlan &p, const LookbackWs &ws,
                               cudaStream_t stream) {
-    using C = SelCfg<IO, kSelDC>;
+    using C = SelCfg<IO, kSelDC, kSelLPC>;
     const int n_db = static_cast<int>((D + C::DC - 1) / C::DC);
     const int64_t grid = p.n_cb * p.S;
-    selective_scan_kernel<IO, kSelDC, ACC, HZ, SP>
+    selective_scan_kernel<IO, kSelDC, kSelLPC, ACC, HZ, SP>
         <<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(
             mx, mdt, mz, mB, mC, A_log, Dskip, h0, static_cast<IO *>(y), h_final,
             static_cast<int>(L), static_cast<int>(D), n_db, p.S, p.tps, p.n_tiles, ws,
@@ -943,7 +955,7 @@ static int selective_launch_t(const void *x, const void *dt, const void *z, cons
                               const float *h0, void *y, float *h_final, int64_t B, int64_t L,
                               int64_t D, int dt_softplus, const DiagPlan &p, void *workspace,
                               cudaStream_t stream) {
-    using C = SelCfg<IO, kSelDC>;
+    using C = SelCfg<IO, kSelDC, kSelLPC>;
     CUtensorMap mx, mdt, mz, mB, mC;
     const auto tt = Io<IO>::kTmType;
     if (!make_map_3d(&mx, x, tt, sizeof(IO), D, L, B, C::DC, C::T) ||
