@@ -221,7 +221,7 @@ __device__ __forceinline__ void rglru_tile(const IO *xs, const IO *rs, const IO 
 }
 
 template <typename IO, bool ACC>
-__global__ void __launch_bounds__(RgCfg<IO>::THREADS)
+__global__ void __launch_bounds__(RgCfg<IO>::THREADS, 1)  // registers for a whole batch in flight
     rglru_scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_r,
                       const __grid_constant__ CUtensorMap tm_i, const float *__restrict__ a_log,
                       float c, const float *__restrict__ h0, IO *__restrict__ y,
@@ -421,11 +421,28 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
             u[m] = dl[m] * xv[m];
         }
         float dqs[C::BATCH], uqs[C::BATCH];
+        if (LPC == 2) {
+            // the partner lane prepared the other parity of steps: one xor
+            // exchange per value, then pick own / other per step
 #pragma unroll
-        for (int q = 0; q < C::BATCH; ++q) {
-            dqs[q] = __shfl_sync(FULL, dl[q / LPC], g0 | (q % LPC));
-            uqs[q] = __shfl_sync(FULL, u[q / LPC], g0 | (q % LPC));
-            if (MODE == kAggregate) dsum += dqs[q];
+            for (int m = 0; m < OWN; ++m) {
+                const float od = __shfl_xor_sync(FULL, dl[m], 1);
+                const float ou = __shfl_xor_sync(FULL, u[m], 1);
+                dqs[2 * m] = r == 0 ? dl[m] : od;
+                dqs[2 * m + 1] = r == 0 ? od : dl[m];
+                uqs[2 * m] = r == 0 ? u[m] : ou;
+                uqs[2 * m + 1] = r == 0 ? ou : u[m];
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < C::BATCH; ++q) {
+                dqs[q] = __shfl_sync(FULL, dl[q / LPC], g0 | (q % LPC));
+                uqs[q] = __shfl_sync(FULL, u[q / LPC], g0 | (q % LPC));
+            }
+        }
+        if (MODE == kAggregate) {
+#pragma unroll
+            for (int q = 0; q < C::BATCH; ++q) dsum += dqs[q];
         }
         float2 ya[C::BATCH];
 #pragma unroll
