@@ -12,25 +12,30 @@
 // The gate decays rows i of S (value channels), so the per-(t, s, i) factor
 // splits through a per-channel reference m[i] (the chunk's mid-range of
 // Lambda): 2^(Lambda_t - Lambda_s) = 2^(Lambda_t - m) 2^(m - Lambda_s).  With
-// V~ = 2^(m - Lambda) (.) V and S~ = diag(2^m) S,
+// V~ = 2^(m - Lambda) (.) V and V~' = 2^(Lambda_C - Lambda) (.) V,
 //
-//   O   = 2^(Lambda - m) (.) ( tril(Q K^T) V~  +  2^m (.) Q S^T )
-//   dS^T = K^T (2^(Lambda_C - Lambda) (.) V)                       (state update, in TMEM)
+//   O    = 2^(Lambda - m) (.) ( tril(Q K^T) V~  +  2^m (.) Q S^T )
+//   dS^T = K^T V~'                                  (state update: S' = 2^Lambda_C (.) S + dS)
 //
-// Four tcgen05 MMAs per chunk (bf16 operands in shared memory, fp32
-// accumulators in tensor memory):
-//   P   = Q K^T            M=64  N=64 K=128   A = Q (K-major),  B = K (K-major)
-//   OX  = Q S^T            M=64  N=32 K=128   B = bf16 state rows (K-major, written by the block)
-//   dSt = K^T V~'          M=128 N=32 K=64    A = the same K tile read MN-major
-//   OI  = tril(P) V~       M=64  N=32 K=64    A = masked P (bf16, written by the block)
-// P and OX of chunk c+1 depend only on its Q, K and the state after chunk c,
-// so they are issued as soon as chunk c's state update is written and run
-// while the block computes chunk c+1's gates.  Q, K (128B-swizzled) and the
-// block's V, g columns arrive by TMA, two chunks in flight.  Rows of S evolve independently (diag(g) scales rows), so a
-// thread block owns 32 value rows of one (batch, head): 4 blocks per head.
-// The fp32 state lives in registers (thread j holds column j of its 32 rows)
-// and is updated elementwise from dS^T; it never leaves the chip between
-// chunks.
+// A thread block owns 64 value rows of one (batch, head) (rows of S evolve
+// independently because diag(g) scales rows): grid = B * H * 2, one block per
+// SM (218 KB of shared memory, all 512 TMEM columns).  Four tcgen05 MMAs per
+// chunk (bf16 operands in shared memory, fp32 accumulators in TMEM):
+//   P    = Q K^T       M=64  N=64 K=128  A = Q (K-major), B = K (K-major), TMA 128B-swizzled
+//   dS^T = K^T V~'     M=128 N=64 K=64   A = the same K tile read MN-major, B = V~' (K-major)
+//   OI   = tril(P) V~  M=64  N=64 K=64   A = masked P (bf16), B = V~ (K-major)
+//   OX   = Q S^T       M=64  N=64 K=128  B = bf16 state, MN-major [key j][value row i]
+// Roles (warp specialised, connected by mbarriers, so consecutive chunks
+// overlap instead of running one serial chain per block):
+//   TMA warp   keeps 3 chunks of Q, K and the block's V, g columns in flight;
+//   MMA warp   one thread issues every MMA and commits it to an mbarrier;
+//   front (4)  gates -> Lambda, m; V~, V~' and 2^(Lambda - m) for chunk c; the
+//              causal mask of P_c (runs up to a chunk ahead of the back);
+//   back (4)   state update S = 2^Lambda_C S + dS (fp32, in registers: thread j
+//              holds key column j of the 64 rows), its bf16 copy for the next
+//              OX, then the outputs of chunk c.
+// TMEM holds two buffers of every accumulator (P, OI, OX, dS: 8 x 64 columns)
+// so the MMAs of chunk c+1 run while the back reads chunk c.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -48,47 +53,83 @@ namespace hg {
 constexpr int C = 64;          // chunk length
 constexpr int DK = 128;        // key channels per head
 constexpr int DV = 128;        // value channels per head
-constexpr int RB = 32;         // value rows of S per thread block
+constexpr int RB = 64;         // value rows of S per thread block
 constexpr int NRB = DV / RB;   // blocks per head
-constexpr int THREADS = 128;
-constexpr int STAGES = 2;
+constexpr int KW = 4;          // back warps 0..3
+constexpr int FW = 4;          // front warps 4..7
+constexpr int TMA_WARP = KW + FW, MMA_WARP = KW + FW + 1;
+constexpr int THREADS = 32 * (KW + FW + 2);
+constexpr int NST = 3;         // TMA stages
 // largest per-chunk spread of Lambda (log2 units) the reference split keeps
 // inside fp32 range with headroom: 2^(+-80) factors
 constexpr float kMaxSpread = 160.0f;
 
-constexpr uint32_t Q_BYTES = C * DK * 2;   // two 64-column 128B-swizzled halves
-constexpr uint32_t VG_BYTES = C * RB * 2;  // plain rows of 32 bf16
-constexpr uint32_t STAGE_BYTES = 2 * Q_BYTES + 2 * VG_BYTES;
-constexpr uint32_t OFF_P = STAGES * STAGE_BYTES;   // masked P, [64 t][64 s] swizzled
-constexpr uint32_t OFF_VT = OFF_P + 8192;          // V~ as [32 i][64 s] swizzled
-constexpr uint32_t OFF_VTP = OFF_VT + 4096;        // V~' as [32 i][64 s] swizzled
-constexpr uint32_t OFF_SB = OFF_VTP + 4096;        // bf16 state rows [32 i][128 j], two swizzled halves
-constexpr uint32_t OFF_LAM = OFF_SB + 8192;        // 2^(Lambda - m), float [64][32], 16-byte groups XOR-swizzled
-constexpr uint32_t OFF_TOT = OFF_LAM + 8192;       // per-warp partial sums, float [4][32]
-constexpr uint32_t OFF_L0 = OFF_TOT + 512;         // Lambda_0, float [32]
-constexpr uint32_t OFF_M = OFF_L0 + 128;           // m, float [32]
-constexpr uint32_t OFF_LC = OFF_M + 128;           // 2^Lambda_C, float [32]
-constexpr uint32_t OFF_BAR = OFF_LC + 128;         // full[2], bar_p, bar_o
-constexpr uint32_t OFF_TMEM = OFF_BAR + 32;
-constexpr uint32_t SMEM = OFF_TMEM + 16;
-static_assert(OFF_P % 1024 == 0 && OFF_VT % 1024 == 0 && OFF_VTP % 1024 == 0 &&
-                  OFF_SB % 1024 == 0 && STAGE_BYTES % 1024 == 0,
+// stage: Q [64 t][128 j] and K [64 s][128 j] as two 128B-swizzled 64-column
+// halves each; V and g [64 t][64 i] as plain bf16 rows
+constexpr uint32_t QK_BYTES = C * DK * 2;
+constexpr uint32_t VG_BYTES = C * RB * 2;
+constexpr uint32_t OFF_K = QK_BYTES, OFF_V = 2 * QK_BYTES, OFF_G = OFF_V + VG_BYTES;
+constexpr uint32_t STAGE_BYTES = 2 * QK_BYTES + 2 * VG_BYTES;
+constexpr uint32_t OFF_PS = NST * STAGE_BYTES;     // masked P [64 t][64 s], swizzled
+constexpr uint32_t OFF_VT = OFF_PS + 8192;         // V~  [64 i][64 s], swizzled
+constexpr uint32_t OFF_VTP = OFF_VT + 8192;        // V~' [64 i][64 s], swizzled
+constexpr uint32_t OFF_SBT = OFF_VTP + 8192;       // bf16 state [128 j][64 i], swizzled
+constexpr uint32_t OFF_E1 = OFF_SBT + 16384;       // 2 x 2^(Lambda - m), fp32 [64 t][64 i]
+constexpr uint32_t OFF_EM = OFF_E1 + 2 * 16384;    // 2 x 2^m [64]
+constexpr uint32_t OFF_GC = OFF_EM + 2 * 256;      // 2 x 2^Lambda_C [64]
+constexpr uint32_t OFF_TOT = OFF_GC + 2 * 256;     // front: first-half totals [64]
+constexpr uint32_t OFF_L0 = OFF_TOT + 256;         // front: Lambda_0 [64]
+constexpr uint32_t OFF_LC = OFF_L0 + 256;          // front: Lambda_C [64]
+constexpr uint32_t OFF_BAR = OFF_LC + 256;
+// full[3] empty[3] bar_p[2] bar_o[2] bar_x[2] fdone[2] kdone[2] sbready mma_done
+constexpr int NBAR = 3 + 3 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
+constexpr uint32_t OFF_FLAG = OFF_TMEM + 8;
+constexpr uint32_t SMEM = OFF_FLAG + 8;
+static_assert(STAGE_BYTES % 1024 == 0 && OFF_PS % 1024 == 0 && OFF_VT % 1024 == 0 &&
+                  OFF_VTP % 1024 == 0 && OFF_SBT % 1024 == 0 && OFF_E1 % 16 == 0,
               "swizzled operand tiles must be 1024-byte aligned");
+static_assert(SMEM <= 227 * 1024, "one block per SM");
 
-constexpr uint32_t TMEM_COLS = 256;  // two blocks per SM fill the 512 columns exactly
-constexpr uint32_t T_P = 0, T_OI = 64, T_OX = 96, T_S = 128;   // accumulator columns
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t T_P = 0, T_OI = 128, T_OX = 256, T_DS = 384;   // + 64 * buffer
 
 constexpr uint32_t IDESC_P = umma_idesc_bf16(64, 64, 0, 0);
-constexpr uint32_t IDESC_O = umma_idesc_bf16(64, RB, 0, 0);
-constexpr uint32_t IDESC_S = umma_idesc_bf16(128, RB, 1, 0);
-// Lambda[t][i] lives at a row-wise XOR swizzle of 4-float groups, so 16 lanes
-// reading 16 rows at the same channel group hit 8 different bank groups.
-__device__ __forceinline__ int lam_index(int t, int i) {
-    return t * RB + ((((i >> 2) ^ (t & 7))) << 2) + (i & 3);
+constexpr uint32_t IDESC_OI = umma_idesc_bf16(64, 64, 0, 0);
+constexpr uint32_t IDESC_OX = umma_idesc_bf16(64, 64, 0, 1);
+constexpr uint32_t IDESC_DS = umma_idesc_bf16(128, 64, 1, 0);
+
+// 2^(Lambda - m)[t][i] with 16-byte groups XOR-swizzled by the row, so the
+// 16 lanes of an epilogue warp (16 consecutive rows, same columns) hit 16
+// different bank groups.
+__device__ __forceinline__ int e1_index(int t, int i) {
+    return t * RB + ((((i >> 2) ^ (t & 15))) << 2) + (i & 3);
+}
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also ORs a predicate over its threads.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1 : 0), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&p);
 }
 }  // namespace hg
 
-__global__ void __launch_bounds__(hg::THREADS)
+__global__ void __launch_bounds__(hg::THREADS, 1)
     hgrn2_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                        const float *__restrict__ S0, float *__restrict__ S_final,
@@ -107,27 +148,33 @@ __global__ void __launch_bounds__(hg::THREADS)
     const int qcol = h * DK, vcol = h * DV + rb * RB;
     const int HV = H * DV;
 
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *bar_p = full + 2;
-    uint64_t *bar_o = full + 3;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    uint64_t *full = bars, *empty = bars + 3, *bar_p = bars + 6, *bar_o = bars + 8,
+             *bar_x = bars + 10, *fdone = bars + 12, *kdone = bars + 14, *sbready = bars + 16,
+             *mma_done = bars + 17;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
-    float *LAM = reinterpret_cast<float *>(sm + OFF_LAM);  // 2^(Lambda - m) per [t][i]
-    float *TOT = reinterpret_cast<float *>(sm + OFF_TOT);
-    float *L0S = reinterpret_cast<float *>(sm + OFF_L0);
-    float *MS = reinterpret_cast<float *>(sm + OFF_M);
-    float *LCS = reinterpret_cast<float *>(sm + OFF_LC);
-    unsigned char *Ps = sm + OFF_P, *VT = sm + OFF_VT, *VTP = sm + OFF_VTP, *SB = sm + OFF_SB;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_FLAG);
+    float *E1 = reinterpret_cast<float *>(sm + OFF_E1);
+    float *EM = reinterpret_cast<float *>(sm + OFF_EM);
+    float *GC = reinterpret_cast<float *>(sm + OFF_GC);
+    unsigned char *Ps = sm + OFF_PS, *VT = sm + OFF_VT, *VTP = sm + OFF_VTP, *SBT = sm + OFF_SBT;
 
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
-        mbar_init(bar_p, 1);
-        mbar_init(bar_o, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 2);   // the MMA commit and the front
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&bar_p[k], 1);
+            mbar_init(&bar_o[k], 1);
+            mbar_init(&bar_x[k], 1);
+            mbar_init(&fdone[k], 1);
+            mbar_init(&kdone[k], KW);
+        }
+        mbar_init(sbready, 1);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        prefetch_tensormap(&tm_g);
     }
     if (warp == 0) tmem_alloc(tmem_slot, TMEM_COLS);
     tc_fence_before();
@@ -135,245 +182,304 @@ __global__ void __launch_bounds__(hg::THREADS)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // state rows rb*32 .. rb*32+31 of S[b, h]; this thread holds column j = tid
-    const size_t srow0 = (size_t(b) * H + h) * DV + size_t(rb) * RB;
-    float S[RB];
-#pragma unroll
-    for (int i = 0; i < RB; ++i) S[i] = S0 != nullptr ? S0[(srow0 + i) * DK + tid] : 0.0f;
-
-    auto issue = [&](int c, int st) {  // thread 0: TMA for chunk c into stage st
-        unsigned char *stg = sm + st * STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
-        tma_load_3d(stg, &tm_q, &full[st], qcol, c * C, b);
-        tma_load_3d(stg + 8192, &tm_q, &full[st], qcol + 64, c * C, b);
-        tma_load_3d(stg + Q_BYTES, &tm_k, &full[st], qcol, c * C, b);
-        tma_load_3d(stg + Q_BYTES + 8192, &tm_k, &full[st], qcol + 64, c * C, b);
-        tma_load_3d(stg + 2 * Q_BYTES, &tm_v, &full[st], vcol, c * C, b);
-        tma_load_3d(stg + 2 * Q_BYTES + VG_BYTES, &tm_g, &full[st], vcol, c * C, b);
-    };
-    // thread 0: P = Q K^T and OX = Q S^T for the chunk whose inputs sit in stage st
-    auto issue_p_ox = [&](int st) {
-        const uint32_t sQ = smem_u32(sm + st * STAGE_BYTES), sK = sQ + Q_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < DK / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-            umma_bf16(tmem + T_P, umma_smem_desc(sQ + off, 16, 1024),
-                      umma_smem_desc(sK + off, 16, 1024), IDESC_P, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < DK / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-            umma_bf16(tmem + T_OX, umma_smem_desc(sQ + off, 16, 1024),
-                      umma_smem_desc(smem_u32(SB) + (kk >> 2) * 4096 + (kk & 3) * 32, 16, 1024),
-                      IDESC_O, kk > 0);
-        }
-        umma_commit(bar_p);
-    };
-    // bf16 copy of the state rows [i][j] (K-major B operand of Q S^T)
-    auto write_state_bf16 = [&]() {
-        const int j = tid, hj = j >> 6, jc = j & 63;
-#pragma unroll
-        for (int i = 0; i < RB; ++i)
-            *reinterpret_cast<__nv_bfloat16 *>(SB + hj * 4096 + sw128_offset(i, jc)) =
-                __float2bfloat16_rn(S[i]);
-    };
-
-    write_state_bf16();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        issue(0, 0);
-        if (n_chunks > 1) issue(1, 1);
-        if (mbar_wait_bounded(&full[0], 0, timeout_ns)) {
-            tc_fence_after();
-            issue_p_ox(0);
-        }
-    }
-
-    for (int c = 0; c < n_chunks; ++c) {
-        const int st = c & 1;
-        unsigned char *stg = sm + st * STAGE_BYTES;
-        const uint32_t sK = smem_u32(stg) + Q_BYTES;
-        const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(stg + 2 * Q_BYTES);
-        const __nv_bfloat16 *sG = sV + C * RB;
-        const int t0 = c * C;
-
-        const bool ok_in = mbar_wait_bounded(&full[st], (c >> 1) & 1, timeout_ns);
-        if (__syncthreads_or(!ok_in)) {
-            if (tid == 0) hg_report(LR_ERR_TIMEOUT);
-            break;
-        }
-
-        // ---- cumulative log2 gates: warp w takes rows 16w..16w+15, lane = value channel
-        float loc[16];
-        {
-            float acc = 0.0f;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int t = 16 * warp + u;
-                const float gv = __bfloat162float(sG[t * RB + lane]);
-                acc += t0 + t < L ? lg2_approx(gv) : 0.0f;  // rows past L: g = 1
-                loc[u] = acc;
+    // Bounded wait; the first wait to run out sets the block's abort flag so
+    // that every role leaves its loop instead of waiting out its own limit.
+    auto hw = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar, parity)) {
+            if (*abort_flag != 0) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1;
+                hg_report(LR_ERR_TIMEOUT);
+                return false;
             }
-            TOT[warp * 32 + lane] = acc;
-            if (warp == 0) L0S[lane] = loc[0];
         }
-        __syncthreads();
+        return true;
+    };
 
-        // ---- causal mask of P = Q K^T (issued at the end of the previous chunk)
-        bool ok = mbar_wait_bounded(bar_p, c & 1, timeout_ns);
-        tc_fence_after();
-        {
-            const uint32_t ta = tmem + T_P + (uint32_t(warp * 32) << 16);
-            const int t = 16 * warp + lane;  // valid for lane < 16 (M = 64 layout)
-            float pa[32], pb[32];
-            tmem_ld32_nowait(ta, pa);
-            tmem_ld32_nowait(ta + 32, pb);
-            tmem_ld_wait();
-            if (lane < 16) {
+    if (warp == TMA_WARP) {  // ------------------------------------------- TMA
+        if (lane == 0) {
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_g);
+            int c = 0;
+            for (; c < n_chunks; ++c) {
+                const int st = c % NST;
+                if (c >= NST && !hw(&empty[st], ((c - NST) / NST) & 1)) break;
+                unsigned char *stg = sm + st * STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
+                tma_load_3d(stg, &tm_q, &full[st], qcol, c * C, b);
+                tma_load_3d(stg + 8192, &tm_q, &full[st], qcol + 64, c * C, b);
+                tma_load_3d(stg + OFF_K, &tm_k, &full[st], qcol, c * C, b);
+                tma_load_3d(stg + OFF_K + 8192, &tm_k, &full[st], qcol + 64, c * C, b);
+                tma_load_3d(stg + OFF_V, &tm_v, &full[st], vcol, c * C, b);
+                tma_load_3d(stg + OFF_G, &tm_g, &full[st], vcol, c * C, b);
+            }
+            // copies still in flight land before the block exits
+            for (int k = c > NST ? c - NST : 0; k < c; ++k)
+                mbar_wait_bounded(&full[k % NST], (k / NST) & 1, timeout_ns);
+        }
+    } else if (warp == MMA_WARP) {  // ------------------------------------- MMA
+        if (lane == 0) {
+            auto issue_p = [&](int c) {  // P_c = Q_c K_c^T into buffer c & 1
+                const uint32_t sQ = smem_u32(sm + (c % NST) * STAGE_BYTES), sK = sQ + OFF_K;
 #pragma unroll
-                for (int chunk = 0; chunk < 8; ++chunk) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s0 = chunk * 8 + 2 * e;
-                        const float v0 = s0 < 32 ? pa[s0] : pb[s0 - 32];
-                        const float v1 = s0 + 1 < 32 ? pa[s0 + 1] : pb[s0 + 1 - 32];
-                        __nv_bfloat162 pr = __floats2bfloat162_rn(s0 <= t ? v0 : 0.0f,
-                                                                  s0 + 1 <= t ? v1 : 0.0f);
-                        w4[e] = *reinterpret_cast<uint32_t *>(&pr);
-                    }
-                    *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                    umma_bf16(tmem + T_P + (c & 1) * 64, umma_smem_desc(sQ + off, 16, 1024),
+                              umma_smem_desc(sK + off, 16, 1024), IDESC_P, kk > 0);
                 }
-            }
-        }
-
-        // ---- Lambda, reference m, V~ and V~'
-        {
-            float off = 0.0f, lc = 0.0f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float tw = TOT[w * 32 + lane];
-                off += w < warp ? tw : 0.0f;
-                lc += tw;
-            }
-            const float l0 = L0S[lane];
-            const float m = 0.5f * (l0 + lc);
-            if (warp == 0 && !(l0 - lc <= kMaxSpread)) hg_report(LR_ERR_RANGE);
-            // 2^(Lambda_C - Lambda) = 2^(m - Lambda) 2^(Lambda_C - m); both factors stay
-            // inside fp32 range because |Lambda - m| and |Lambda_C - m| are at most 80
-            const float cm = ex2_approx(lc - m);
-            uint32_t vt[8], vtp[8];  // bf16 pairs of this lane's row, columns 16w .. 16w+15
-#pragma unroll
-            for (int u = 0; u < 16; u += 2) {
-                const int t = 16 * warp + u;
-                const float lam0 = loc[u] + off, lam1 = loc[u + 1] + off;
-                LAM[lam_index(t, lane)] = ex2_approx(lam0 - m);
-                LAM[lam_index(t + 1, lane)] = ex2_approx(lam1 - m);
-                const float v0 = __bfloat162float(sV[t * RB + lane]);
-                const float v1 = __bfloat162float(sV[(t + 1) * RB + lane]);
-                const float w0 = ex2_approx(m - lam0) * v0, w1 = ex2_approx(m - lam1) * v1;
-                __nv_bfloat162 a = __floats2bfloat162_rn(w0, w1);
-                __nv_bfloat162 bq = __floats2bfloat162_rn(w0 * cm, w1 * cm);
-                vt[u / 2] = *reinterpret_cast<uint32_t *>(&a);
-                vtp[u / 2] = *reinterpret_cast<uint32_t *>(&bq);
-            }
-#pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {   // two 16-byte chunks: columns 16w + 8*h8 ..
-                const uint32_t off8 = sw128_offset(lane, 16 * warp + 8 * h8);
-                *reinterpret_cast<uint4 *>(VT + off8) =
-                    make_uint4(vt[4 * h8], vt[4 * h8 + 1], vt[4 * h8 + 2], vt[4 * h8 + 3]);
-                *reinterpret_cast<uint4 *>(VTP + off8) =
-                    make_uint4(vtp[4 * h8], vtp[4 * h8 + 1], vtp[4 * h8 + 2], vtp[4 * h8 + 3]);
-            }
-            if (warp == 0) {
-                MS[lane] = ex2_approx(m);
-                LCS[lane] = ex2_approx(lc);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) hg_report(LR_ERR_TIMEOUT);
-            break;
-        }
-        if (tid == 0) {
-            tc_fence_after();
-            // dS^T = K^T V~'  (K tile read MN-major: 64-column halves 8 KB apart)
-#pragma unroll
-            for (int kk = 0; kk < C / 16; ++kk)
-                umma_bf16(tmem + T_S, umma_smem_desc(sK + kk * 2048, 8192, 1024),
-                          umma_smem_desc(smem_u32(VTP) + kk * 32, 16, 1024), IDESC_S, kk > 0);
-            // OI = tril(P) V~
-#pragma unroll
-            for (int kk = 0; kk < C / 16; ++kk)
-                umma_bf16(tmem + T_OI, umma_smem_desc(smem_u32(Ps) + kk * 32, 16, 1024),
-                          umma_smem_desc(smem_u32(VT) + kk * 32, 16, 1024), IDESC_O, kk > 0);
-            umma_commit(bar_o);
-        }
-        ok = mbar_wait_bounded(bar_o, c & 1, timeout_ns);
-        tc_fence_after();
-        {   // ---- output rows: o_t = 2^(Lambda_t - m) (OI_t + 2^m OX_t)
-            const uint32_t lw = uint32_t(warp * 32) << 16;
-            const int t = 16 * warp + lane;
-            float oi[32], ox[32];
-            tmem_ld32_nowait(tmem + T_OI + lw, oi);
-            tmem_ld32_nowait(tmem + T_OX + lw, ox);
-            tmem_ld_wait();
-            if (lane < 16 && t0 + t < L) {
-                uint4 w4[4];
-                uint32_t *wp = reinterpret_cast<uint32_t *>(w4);
-#pragma unroll
-                for (int i = 0; i < RB; i += 4) {
-                    const float4 e1 = *reinterpret_cast<const float4 *>(LAM + lam_index(t, i));
-                    const float4 em = *reinterpret_cast<const float4 *>(MS + i);
-                    const float r0 = fmaf(em.x, ox[i], oi[i]) * e1.x;
-                    const float r1 = fmaf(em.y, ox[i + 1], oi[i + 1]) * e1.y;
-                    const float r2 = fmaf(em.z, ox[i + 2], oi[i + 2]) * e1.z;
-                    const float r3 = fmaf(em.w, ox[i + 3], oi[i + 3]) * e1.w;
-                    __nv_bfloat162 p0 = __floats2bfloat162_rn(r0, r1);
-                    __nv_bfloat162 p1 = __floats2bfloat162_rn(r2, r3);
-                    wp[i / 2] = *reinterpret_cast<uint32_t *>(&p0);
-                    wp[i / 2 + 1] = *reinterpret_cast<uint32_t *>(&p1);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(o + (size_t(b) * L + t0 + t) * HV + vcol);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) dst[q] = w4[q];
-            }
-        }
-        {   // ---- state: S = diag(2^Lambda_C) S + dS, and its bf16 copy for the next chunk
-            const uint32_t ta = tmem + T_S + (uint32_t(warp * 32) << 16);
-            float ds[32];
-            tmem_ld32_nowait(ta, ds);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < RB; ++i) S[i] = fmaf(LCS[i], S[i], ds[i]);
-            write_state_bf16();
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) hg_report(LR_ERR_TIMEOUT);
-            break;
-        }
-        if (tid == 0) {
-            if (c + 2 < n_chunks) issue(c + 2, st);
-            if (c + 1 < n_chunks &&
-                mbar_wait_bounded(&full[(c + 1) & 1], ((c + 1) >> 1) & 1, timeout_ns)) {
+                umma_commit(&bar_p[c & 1]);
+            };
+            bool ok = n_chunks > 0 && hw(&full[0], 0);
+            if (ok) {
                 tc_fence_after();
-                issue_p_ox((c + 1) & 1);
+                issue_p(0);
             }
+            for (int c = 0; ok && c < n_chunks; ++c) {
+                const int st = c % NST, bi = c & 1;
+                const uint32_t sQ = smem_u32(sm + st * STAGE_BYTES), sK = sQ + OFF_K;
+                // P of the next chunk: its buffer held P_{c-1}, masked once the
+                // front finished chunk c-1
+                if (c + 1 < n_chunks) {
+                    if (!hw(&full[(c + 1) % NST], ((c + 1) / NST) & 1)) break;
+                    if (c >= 1 && !hw(&fdone[(c - 1) & 1], ((c - 1) >> 1) & 1)) break;
+                    tc_fence_after();
+                    issue_p(c + 1);
+                }
+                // dS_c and OI_c once the front wrote V~', V~ and the masked P of
+                // chunk c and the back released the accumulators of chunk c-2
+                if (!hw(&fdone[bi], (c >> 1) & 1)) break;
+                if (c >= 2 && !hw(&kdone[bi], ((c - 2) >> 1) & 1)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C / 16; ++kk)
+                    umma_bf16(tmem + T_DS + bi * 64, umma_smem_desc(sK + kk * 2048, 8192, 1024),
+                              umma_smem_desc(smem_u32(VTP) + kk * 32, 16, 1024), IDESC_DS, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < C / 16; ++kk)
+                    umma_bf16(tmem + T_OI + bi * 64, umma_smem_desc(smem_u32(Ps) + kk * 32, 16, 1024),
+                              umma_smem_desc(smem_u32(VT) + kk * 32, 16, 1024), IDESC_OI, kk > 0);
+                umma_commit(&bar_o[bi]);
+                // OX_c = Q_c S^T once the back wrote the bf16 state after chunk c-1
+                if (!hw(sbready, c & 1)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint32_t qoff = (kk >> 2) * 8192 + (kk & 3) * 32;
+                    umma_bf16(tmem + T_OX + bi * 64, umma_smem_desc(sQ + qoff, 16, 1024),
+                              umma_smem_desc(smem_u32(SBT) + kk * 2048, 8192, 1024), IDESC_OX, kk > 0);
+                }
+                umma_commit(&bar_x[bi]);
+                umma_commit(&empty[st]);   // Q_c, K_c are no longer read once these complete
+            }
+            // nothing of this block's may still run on the tensor cores when
+            // its TMEM is released
+            umma_commit(mma_done);
+            mbar_wait_bounded(mma_done, 0, timeout_ns);
+        }
+    } else if (warp >= KW) {  // ----------------------------------------- front
+        const int f = tid - 32 * KW, fw = warp - KW;
+        const int i = f & (RB - 1), hf = f / RB;   // value row, half of the chunk's steps
+        const int tb = 32 * hf;
+        float *TOTF = reinterpret_cast<float *>(sm + OFF_TOT);
+        float *L0F = reinterpret_cast<float *>(sm + OFF_L0);
+        float *LCF = reinterpret_cast<float *>(sm + OFF_LC);
+        for (int c = 0; c < n_chunks; ++c) {
+            const int st = c % NST, bi = c & 1;
+            const unsigned char *stg = sm + st * STAGE_BYTES;
+            const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(stg + OFF_V);
+            const __nv_bfloat16 *sG = reinterpret_cast<const __nv_bfloat16 *>(stg + OFF_G);
+            // inputs landed; 2^(Lambda - m) buffer free (back done with chunk
+            // c-2); V~, V~', P buffers free (dS, OI of chunk c-1 done)
+            bool ok = hw(&full[st], (c / NST) & 1);
+            if (ok && c >= 2) ok = hw(&kdone[bi], ((c - 2) >> 1) & 1);
+            if (ok && c >= 1) ok = hw(&bar_o[(c - 1) & 1], ((c - 1) >> 1) & 1);
+            if (named_bar_or(2, 32 * FW, !ok)) break;
+
+            // cumulative log2 gates over this thread's 32 steps (steps past L: g = 1)
+            const int t0 = c * C;
+            float loc[32];
+            {
+                float acc = 0.0f;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int t = tb + u;
+                    const float gv = __bfloat162float(sG[t * RB + i]);
+                    acc += t0 + t < L ? lg2_approx(gv) : 0.0f;
+                    loc[u] = acc;
+                }
+                if (hf == 0) {
+                    TOTF[i] = acc;
+                    L0F[i] = loc[0];
+                }
+                named_bar(2, 32 * FW);
+                const float off = hf ? TOTF[i] : 0.0f;
+                if (hf == 1) LCF[i] = off + acc;
+#pragma unroll
+                for (int u = 0; u < 32; ++u) loc[u] += off;
+            }
+            named_bar(2, 32 * FW);
+            const float l0 = L0F[i], lc = LCF[i];
+            const float m = 0.5f * (l0 + lc);
+            if (hf == 0 && !(l0 - lc <= kMaxSpread)) hg_report(LR_ERR_RANGE);
+            float *e1 = E1 + bi * (C * RB);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) e1[e1_index(tb + u, i)] = ex2_approx(loc[u] - m);
+            if (hf == 0) {
+                EM[bi * RB + i] = ex2_approx(m);
+                GC[bi * RB + i] = ex2_approx(lc);
+            }
+            {   // V~ = 2^(m - Lambda) v and V~' = 2^(Lambda_C - m) V~ for row i, this half
+                const float cm = ex2_approx(lc - m);
+                uint32_t vt[16], vtp[16];
+#pragma unroll
+                for (int u = 0; u < 32; u += 2) {
+                    const int t = tb + u;
+                    const float w0 = ex2_approx(m - loc[u]) * __bfloat162float(sV[t * RB + i]);
+                    const float w1 = ex2_approx(m - loc[u + 1]) * __bfloat162float(sV[(t + 1) * RB + i]);
+                    vt[u / 2] = pack_bf16(w0, w1);
+                    vtp[u / 2] = pack_bf16(w0 * cm, w1 * cm);
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t o8 = sw128_offset(i, tb + 8 * k);
+                    *reinterpret_cast<uint4 *>(VT + o8) =
+                        make_uint4(vt[4 * k], vt[4 * k + 1], vt[4 * k + 2], vt[4 * k + 3]);
+                    *reinterpret_cast<uint4 *>(VTP + o8) =
+                        make_uint4(vtp[4 * k], vtp[4 * k + 1], vtp[4 * k + 2], vtp[4 * k + 3]);
+                }
+            }
+            // causal mask of P_c (M = 64 rows t sit in lanes 0..15 of each warp quarter)
+            ok = hw(&bar_p[bi], (c >> 1) & 1);
+            if (named_bar_or(2, 32 * FW, !ok)) break;
+            tc_fence_after();
+            {
+                const uint32_t ta = tmem + T_P + bi * 64 + (uint32_t(fw * 32) << 16);
+                float pa[32], pb[32];
+                tmem_ld32_nowait(ta, pa);
+                tmem_ld32_nowait(ta + 32, pb);
+                tmem_ld_wait_tied(pa);
+                tmem_ld_wait_tied(pb);
+                const int t = 16 * fw + lane;
+                if (lane < 16) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s0 = ch * 8 + 2 * e;
+                            const float v0 = s0 < 32 ? pa[s0] : pb[s0 - 32];
+                            const float v1 = s0 + 1 < 32 ? pa[s0 + 1] : pb[s0 + 1 - 32];
+                            w4[e] = pack_bf16(s0 <= t ? v0 : 0.0f, s0 + 1 <= t ? v1 : 0.0f);
+                        }
+                        *reinterpret_cast<uint4 *>(Ps + t * 128 + ((ch ^ (t & 7)) << 4)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar(2, 32 * FW);
+            if (f == 0) {
+                arrive(&fdone[bi]);
+                arrive(&empty[st]);   // V, g of stage st no longer read
+            }
+        }
+    } else {  // ------------------------------------------------------------ back
+        // key column j = tid of value rows rb*64 .. rb*64+63 of S[b, h]
+        const size_t srow0 = size_t(bh) * DV + size_t(rb) * RB;
+        float S[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) S[r] = S0 != nullptr ? S0[(srow0 + r) * DK + tid] : 0.0f;
+        // bf16 copy, MN-major: row j holds the 64 value rows in 8 swizzled 16-byte groups
+        auto write_state = [&]() {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<uint4 *>(SBT + sw128_offset(tid, 8 * k)) =
+                    make_uint4(pack_bf16(S[8 * k], S[8 * k + 1]), pack_bf16(S[8 * k + 2], S[8 * k + 3]),
+                               pack_bf16(S[8 * k + 4], S[8 * k + 5]), pack_bf16(S[8 * k + 6], S[8 * k + 7]));
+            fence_proxy_async_smem();
+            named_bar(1, 32 * KW);
+            if (tid == 0) arrive(sbready);
+        };
+        write_state();
+        const uint32_t lanes = uint32_t(warp * 32) << 16;
+        for (int c = 0; c < n_chunks; ++c) {
+            const int bi = c & 1;
+            bool ok = hw(&fdone[bi], (c >> 1) & 1);
+            if (ok) ok = hw(&bar_o[bi], (c >> 1) & 1);
+            if (named_bar_or(1, 32 * KW, !ok)) break;
+            tc_fence_after();
+            {   // S = diag(2^Lambda_C) S + dS   (dS^T lane j, column i)
+                const float *gc = GC + bi * RB;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float ds[32];
+                    tmem_ld32_nowait(tmem + T_DS + bi * 64 + 32 * hh + lanes, ds);
+                    tmem_ld_wait_tied(ds);
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(gc + 32 * hh + q);
+                        S[32 * hh + q] = fmaf(g4.x, S[32 * hh + q], ds[q]);
+                        S[32 * hh + q + 1] = fmaf(g4.y, S[32 * hh + q + 1], ds[q + 1]);
+                        S[32 * hh + q + 2] = fmaf(g4.z, S[32 * hh + q + 2], ds[q + 2]);
+                        S[32 * hh + q + 3] = fmaf(g4.w, S[32 * hh + q + 3], ds[q + 3]);
+                    }
+                }
+            }
+            // OX_c reads the previous bf16 state until bar_x
+            ok = hw(&bar_x[bi], (c >> 1) & 1);
+            if (named_bar_or(1, 32 * KW, !ok)) break;
+            tc_fence_after();
+            write_state();
+            {   // outputs: o_t = 2^(Lambda_t - m) (OI_t + 2^m OX_t), row t = 16 warp + lane
+                const int t = 16 * warp + lane;
+                const float *e1 = E1 + bi * (C * RB);
+                const float *em = EM + bi * RB;
+                const bool store = lane < 16 && c * C + t < L;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float oi[32], ox[32];
+                    tmem_ld32_nowait(tmem + T_OI + bi * 64 + 32 * hh + lanes, oi);
+                    tmem_ld32_nowait(tmem + T_OX + bi * 64 + 32 * hh + lanes, ox);
+                    tmem_ld_wait_tied(oi);
+                    tmem_ld_wait_tied(ox);
+                    if (store) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int q = 0; q < 32; q += 4) {
+                            const int i0 = 32 * hh + q;
+                            const float4 e = *reinterpret_cast<const float4 *>(e1 + e1_index(t, i0));
+                            const float4 mm = *reinterpret_cast<const float4 *>(em + i0);
+                            w[q / 2] = pack_bf16(fmaf(mm.x, ox[q], oi[q]) * e.x,
+                                                 fmaf(mm.y, ox[q + 1], oi[q + 1]) * e.y);
+                            w[q / 2 + 1] = pack_bf16(fmaf(mm.z, ox[q + 2], oi[q + 2]) * e.z,
+                                                     fmaf(mm.w, ox[q + 3], oi[q + 3]) * e.w);
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(o + (size_t(b) * L + c * C + t) * HV +
+                                                               vcol + 32 * hh);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive(&kdone[bi]);
+        }
+        if (S_final != nullptr) {
+#pragma unroll
+            for (int r = 0; r < RB; ++r) S_final[(srow0 + r) * DK + tid] = S[r];
         }
     }
 
-    if (S_final != nullptr) {
-#pragma unroll
-        for (int i = 0; i < RB; ++i) S_final[(srow0 + i) * DK + tid] = S[i];
-    }
     tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
 }
 
