@@ -29,8 +29,10 @@
 // overlap instead of running one serial chain per block):
 //   TMA warp   keeps 3 chunks of Q, K and the block's V, g columns in flight;
 //   MMA warp   one thread issues every MMA and commits it to an mbarrier;
-//   front (4)  gates -> Lambda, m; V~, V~' and 2^(Lambda - m) for chunk c; the
-//              causal mask of P_c (runs up to a chunk ahead of the back);
+//   front (8)  gates -> Lambda, m; V~, V~' and 2^(Lambda - m) for chunk c; the
+//              causal mask of P_c (runs up to a chunk ahead of the back).  Its
+//              per-element exp2 / log2 chains are the longest per-chunk work,
+//              so it gets two warps per scheduler;
 //   back (4)   state update S = 2^Lambda_C S + dS (fp32, in registers: thread j
 //              holds key column j of the 64 rows), its bf16 copy for the next
 //              OX, then the outputs of chunk c.
@@ -56,7 +58,9 @@ constexpr int DV = 128;        // value channels per head
 constexpr int RB = 64;         // value rows of S per thread block
 constexpr int NRB = DV / RB;   // blocks per head
 constexpr int KW = 4;          // back warps 0..3
-constexpr int FW = 4;          // front warps 4..7
+constexpr int FW = 8;          // front warps 4..11
+constexpr int FQ = FW * 32 / 64;   // front threads per value row = quarters of the chunk's steps
+constexpr int FSTEPS = 64 / FQ;    // steps per front thread
 constexpr int TMA_WARP = KW + FW, MMA_WARP = KW + FW + 1;
 constexpr int THREADS = 32 * (KW + FW + 2);
 constexpr int NST = 3;         // TMA stages
@@ -77,10 +81,9 @@ constexpr uint32_t OFF_SBT = OFF_VTP + 8192;       // bf16 state [128 j][64 i], 
 constexpr uint32_t OFF_E1 = OFF_SBT + 16384;       // 2 x 2^(Lambda - m), fp32 [64 t][64 i]
 constexpr uint32_t OFF_EM = OFF_E1 + 2 * 16384;    // 2 x 2^m [64]
 constexpr uint32_t OFF_GC = OFF_EM + 2 * 256;      // 2 x 2^Lambda_C [64]
-constexpr uint32_t OFF_TOT = OFF_GC + 2 * 256;     // front: first-half totals [64]
-constexpr uint32_t OFF_L0 = OFF_TOT + 256;         // front: Lambda_0 [64]
-constexpr uint32_t OFF_LC = OFF_L0 + 256;          // front: Lambda_C [64]
-constexpr uint32_t OFF_BAR = OFF_LC + 256;
+constexpr uint32_t OFF_TOT = OFF_GC + 2 * 256;     // front: per-quarter totals [FQ][64]
+constexpr uint32_t OFF_L0 = OFF_TOT + FQ * 256;    // front: Lambda_0 [64]
+constexpr uint32_t OFF_BAR = OFF_L0 + 256;
 // full[3] empty[3] bar_p[2] bar_o[2] bar_x[2] fdone[2] kdone[2] sbready mma_done
 constexpr int NBAR = 3 + 3 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
@@ -282,11 +285,10 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
         }
     } else if (warp >= KW) {  // ----------------------------------------- front
         const int f = tid - 32 * KW, fw = warp - KW;
-        const int i = f & (RB - 1), hf = f / RB;   // value row, half of the chunk's steps
-        const int tb = 32 * hf;
+        const int i = f & (RB - 1), qt = f / RB;   // value row, quarter of the chunk's steps
+        const int tb = FSTEPS * qt;
         float *TOTF = reinterpret_cast<float *>(sm + OFF_TOT);
         float *L0F = reinterpret_cast<float *>(sm + OFF_L0);
-        float *LCF = reinterpret_cast<float *>(sm + OFF_LC);
         for (int c = 0; c < n_chunks; ++c) {
             const int st = c % NST, bi = c & 1;
             const unsigned char *stg = sm + st * STAGE_BYTES;
@@ -299,44 +301,44 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             if (ok && c >= 1) ok = hw(&bar_o[(c - 1) & 1], ((c - 1) >> 1) & 1);
             if (named_bar_or(2, 32 * FW, !ok)) break;
 
-            // cumulative log2 gates over this thread's 32 steps (steps past L: g = 1)
+            // cumulative log2 gates over this thread's steps (steps past L: g = 1)
             const int t0 = c * C;
-            float loc[32];
-            {
-                float acc = 0.0f;
+            float loc[FSTEPS];
+            float acc = 0.0f;
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int t = tb + u;
-                    const float gv = __bfloat162float(sG[t * RB + i]);
-                    acc += t0 + t < L ? lg2_approx(gv) : 0.0f;
-                    loc[u] = acc;
-                }
-                if (hf == 0) {
-                    TOTF[i] = acc;
-                    L0F[i] = loc[0];
-                }
-                named_bar(2, 32 * FW);
-                const float off = hf ? TOTF[i] : 0.0f;
-                if (hf == 1) LCF[i] = off + acc;
-#pragma unroll
-                for (int u = 0; u < 32; ++u) loc[u] += off;
+            for (int u = 0; u < FSTEPS; ++u) {
+                const int t = tb + u;
+                const float gv = __bfloat162float(sG[t * RB + i]);
+                acc += t0 + t < L ? lg2_approx(gv) : 0.0f;
+                loc[u] = acc;
             }
+            TOTF[qt * RB + i] = acc;
+            if (qt == 0) L0F[i] = loc[0];
             named_bar(2, 32 * FW);
-            const float l0 = L0F[i], lc = LCF[i];
+            float off = 0.0f, lc = 0.0f;
+#pragma unroll
+            for (int q = 0; q < FQ; ++q) {
+                const float tq = TOTF[q * RB + i];
+                off += q < qt ? tq : 0.0f;
+                lc += tq;
+            }
+#pragma unroll
+            for (int u = 0; u < FSTEPS; ++u) loc[u] += off;
+            const float l0 = L0F[i];
             const float m = 0.5f * (l0 + lc);
-            if (hf == 0 && !(l0 - lc <= kMaxSpread)) hg_report(LR_ERR_RANGE);
+            if (qt == 0 && !(l0 - lc <= kMaxSpread)) hg_report(LR_ERR_RANGE);
             float *e1 = E1 + bi * (C * RB);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) e1[e1_index(tb + u, i)] = ex2_approx(loc[u] - m);
-            if (hf == 0) {
+            for (int u = 0; u < FSTEPS; ++u) e1[e1_index(tb + u, i)] = ex2_approx(loc[u] - m);
+            if (qt == 0) {
                 EM[bi * RB + i] = ex2_approx(m);
                 GC[bi * RB + i] = ex2_approx(lc);
             }
-            {   // V~ = 2^(m - Lambda) v and V~' = 2^(Lambda_C - m) V~ for row i, this half
+            {   // V~ = 2^(m - Lambda) v and V~' = 2^(Lambda_C - m) V~ for row i, these steps
                 const float cm = ex2_approx(lc - m);
-                uint32_t vt[16], vtp[16];
+                uint32_t vt[FSTEPS / 2], vtp[FSTEPS / 2];
 #pragma unroll
-                for (int u = 0; u < 32; u += 2) {
+                for (int u = 0; u < FSTEPS; u += 2) {
                     const int t = tb + u;
                     const float w0 = ex2_approx(m - loc[u]) * __bfloat162float(sV[t * RB + i]);
                     const float w1 = ex2_approx(m - loc[u + 1]) * __bfloat162float(sV[(t + 1) * RB + i]);
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                     vtp[u / 2] = pack_bf16(w0 * cm, w1 * cm);
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < FSTEPS / 8; ++k) {
                     const uint32_t o8 = sw128_offset(i, tb + 8 * k);
                     *reinterpret_cast<uint4 *>(VT + o8) =
                         make_uint4(vt[4 * k], vt[4 * k + 1], vt[4 * k + 2], vt[4 * k + 3]);
@@ -352,30 +354,29 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                         make_uint4(vtp[4 * k], vtp[4 * k + 1], vtp[4 * k + 2], vtp[4 * k + 3]);
                 }
             }
-            // causal mask of P_c (M = 64 rows t sit in lanes 0..15 of each warp quarter)
+            // causal mask of P_c: M = 64 rows t sit in lanes 0..15 of each warp
+            // quarter; the two warps of a quarter take 32 columns s each
             ok = hw(&bar_p[bi], (c >> 1) & 1);
             if (named_bar_or(2, 32 * FW, !ok)) break;
             tc_fence_after();
             {
-                const uint32_t ta = tmem + T_P + bi * 64 + (uint32_t(fw * 32) << 16);
-                float pa[32], pb[32];
-                tmem_ld32_nowait(ta, pa);
-                tmem_ld32_nowait(ta + 32, pb);
-                tmem_ld_wait_tied(pa);
-                tmem_ld_wait_tied(pb);
-                const int t = 16 * fw + lane;
+                const int quarter = fw & 3, s_base = 32 * (fw >> 2);
+                float pv[32];
+                tmem_ld32_nowait(tmem + T_P + bi * 64 + s_base + (uint32_t(quarter * 32) << 16), pv);
+                tmem_ld_wait_tied(pv);
+                const int t = 16 * quarter + lane;
                 if (lane < 16) {
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
+                    for (int ch = 0; ch < 4; ++ch) {
                         uint32_t w4[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int s0 = ch * 8 + 2 * e;
-                            const float v0 = s0 < 32 ? pa[s0] : pb[s0 - 32];
-                            const float v1 = s0 + 1 < 32 ? pa[s0 + 1] : pb[s0 + 1 - 32];
-                            w4[e] = pack_bf16(s0 <= t ? v0 : 0.0f, s0 + 1 <= t ? v1 : 0.0f);
+                            const int s0 = s_base + ch * 8 + 2 * e;
+                            w4[e] = pack_bf16(s0 <= t ? pv[ch * 8 + 2 * e] : 0.0f,
+                                              s0 + 1 <= t ? pv[ch * 8 + 2 * e + 1] : 0.0f);
                         }
-                        *reinterpret_cast<uint4 *>(Ps + t * 128 + ((ch ^ (t & 7)) << 4)) =
+                        const int chunk = (s_base >> 3) + ch;
+                        *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) =
                             make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
                 }
@@ -416,17 +417,24 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             {   // S = diag(2^Lambda_C) S + dS   (dS^T lane j, column i)
                 const float *gc = GC + bi * RB;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float ds[32];
-                    tmem_ld32_nowait(tmem + T_DS + bi * 64 + 32 * hh + lanes, ds);
-                    tmem_ld_wait_tied(ds);
+                for (int hh = 0; hh < 4; hh += 2) {
+                    float d0[16], d1[16];
+                    tmem_ld16_nowait(tmem + T_DS + bi * 64 + 16 * hh + lanes, d0);
+                    tmem_ld16_nowait(tmem + T_DS + bi * 64 + 16 * hh + 16 + lanes, d1);
+                    tmem_ld_wait_tied(d0, d1);
 #pragma unroll
-                    for (int q = 0; q < 32; q += 4) {
-                        const float4 g4 = *reinterpret_cast<const float4 *>(gc + 32 * hh + q);
-                        S[32 * hh + q] = fmaf(g4.x, S[32 * hh + q], ds[q]);
-                        S[32 * hh + q + 1] = fmaf(g4.y, S[32 * hh + q + 1], ds[q + 1]);
-                        S[32 * hh + q + 2] = fmaf(g4.z, S[32 * hh + q + 2], ds[q + 2]);
-                        S[32 * hh + q + 3] = fmaf(g4.w, S[32 * hh + q + 3], ds[q + 3]);
+                    for (int q = 0; q < 16; q += 4) {
+                        const float4 g0 = *reinterpret_cast<const float4 *>(gc + 16 * hh + q);
+                        const float4 g1 = *reinterpret_cast<const float4 *>(gc + 16 * hh + 16 + q);
+                        float *s0 = S + 16 * hh + q, *s1 = S + 16 * hh + 16 + q;
+                        s0[0] = fmaf(g0.x, s0[0], d0[q]);
+                        s0[1] = fmaf(g0.y, s0[1], d0[q + 1]);
+                        s0[2] = fmaf(g0.z, s0[2], d0[q + 2]);
+                        s0[3] = fmaf(g0.w, s0[3], d0[q + 3]);
+                        s1[0] = fmaf(g1.x, s1[0], d1[q]);
+                        s1[1] = fmaf(g1.y, s1[1], d1[q + 1]);
+                        s1[2] = fmaf(g1.z, s1[2], d1[q + 2]);
+                        s1[3] = fmaf(g1.w, s1[3], d1[q + 3]);
                     }
                 }
             }
@@ -441,17 +449,16 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                 const float *em = EM + bi * RB;
                 const bool store = lane < 16 && c * C + t < L;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float oi[32], ox[32];
-                    tmem_ld32_nowait(tmem + T_OI + bi * 64 + 32 * hh + lanes, oi);
-                    tmem_ld32_nowait(tmem + T_OX + bi * 64 + 32 * hh + lanes, ox);
-                    tmem_ld_wait_tied(oi);
-                    tmem_ld_wait_tied(ox);
+                for (int hh = 0; hh < 4; ++hh) {   // 16 value rows i at a time
+                    float oi[16], ox[16];
+                    tmem_ld16_nowait(tmem + T_OI + bi * 64 + 16 * hh + lanes, oi);
+                    tmem_ld16_nowait(tmem + T_OX + bi * 64 + 16 * hh + lanes, ox);
+                    tmem_ld_wait_tied(oi, ox);
                     if (store) {
-                        uint32_t w[16];
+                        uint32_t w[8];
 #pragma unroll
-                        for (int q = 0; q < 32; q += 4) {
-                            const int i0 = 32 * hh + q;
+                        for (int q = 0; q < 16; q += 4) {
+                            const int i0 = 16 * hh + q;
                             const float4 e = *reinterpret_cast<const float4 *>(e1 + e1_index(t, i0));
                             const float4 mm = *reinterpret_cast<const float4 *>(em + i0);
                             w[q / 2] = pack_bf16(fmaf(mm.x, ox[q], oi[q]) * e.x,
@@ -460,10 +467,9 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                                                      fmaf(mm.w, ox[q + 3], oi[q + 3]) * e.w);
                         }
                         uint4 *dst = reinterpret_cast<uint4 *>(o + (size_t(b) * L + c * C + t) * HV +
-                                                               vcol + 32 * hh);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+                                                               vcol + 16 * hh);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                     }
                 }
             }
