@@ -294,11 +294,9 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             const unsigned char *stg = sm + st * STAGE_BYTES;
             const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(stg + OFF_V);
             const __nv_bfloat16 *sG = reinterpret_cast<const __nv_bfloat16 *>(stg + OFF_G);
-            // inputs landed; 2^(Lambda - m) buffer free (back done with chunk
-            // c-2); V~, V~', P buffers free (dS, OI of chunk c-1 done)
+            // inputs landed; 2^(Lambda - m) buffer free (back done with chunk c-2)
             bool ok = hw(&full[st], (c / NST) & 1);
             if (ok && c >= 2) ok = hw(&kdone[bi], ((c - 2) >> 1) & 1);
-            if (ok && c >= 1) ok = hw(&bar_o[(c - 1) & 1], ((c - 1) >> 1) & 1);
             if (named_bar_or(2, 32 * FW, !ok)) break;
 
             // cumulative log2 gates over this thread's steps (steps past L: g = 1)
@@ -345,6 +343,10 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                     vt[u / 2] = pack_bf16(w0, w1);
                     vtp[u / 2] = pack_bf16(w0 * cm, w1 * cm);
                 }
+                // the V~, V~' and masked-P buffers are free once dS and OI of
+                // chunk c-1 completed; the work above overlapped with them
+                ok = c == 0 || hw(&bar_o[(c - 1) & 1], ((c - 1) >> 1) & 1);
+                if (named_bar_or(2, 32 * FW, !ok)) break;
 #pragma unroll
                 for (int k = 0; k < FSTEPS / 8; ++k) {
                     const uint32_t o8 = sw128_offset(i, tb + 8 * k);
