@@ -28,7 +28,10 @@
 // Roles (warp specialised, connected by mbarriers, so consecutive chunks
 // overlap instead of running one serial chain per block):
 //   TMA warp   keeps 3 chunks of Q, K and the block's V, g columns in flight;
-//   MMA warp   one thread issues every MMA and commits it to an mbarrier;
+//   MMA warp   one thread issues P, dS and OI and commits them to mbarriers;
+//   OX warp    one thread issues OX = Q S^T as soon as the back published the
+//              state it needs (a second issuer keeps this state-dependent MMA
+//              from queueing behind the front's work on the next chunk);
 //   front (8)  gates -> Lambda, m; V~, V~' and 2^(Lambda - m) for chunk c; the
 //              causal mask of P_c (runs up to a chunk ahead of the back).  Its
 //              per-element exp2 / log2 chains are the longest per-chunk work,
@@ -61,8 +64,8 @@ constexpr int KW = 4;          // back warps 0..3
 constexpr int FW = 8;          // front warps 4..11
 constexpr int FQ = FW * 32 / 64;   // front threads per value row = quarters of the chunk's steps
 constexpr int FSTEPS = 64 / FQ;    // steps per front thread
-constexpr int TMA_WARP = KW + FW, MMA_WARP = KW + FW + 1;
-constexpr int THREADS = 32 * (KW + FW + 2);
+constexpr int TMA_WARP = KW + FW, MMA_WARP = KW + FW + 1, OX_WARP = KW + FW + 2;
+constexpr int THREADS = 32 * (KW + FW + 3);
 constexpr int NST = 3;         // TMA stages
 // largest per-chunk spread of Lambda (log2 units) the reference split keeps
 // inside fp32 range with headroom: 2^(+-80) factors
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);   // the MMA commit and the front
+            mbar_init(&empty[s], 3);   // the two MMA issuers' commits and the front
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&bar_p[k], 1);
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             mbar_init(&kdone[k], KW);
         }
         mbar_init(sbready, 1);
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -266,9 +269,24 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                     umma_bf16(tmem + T_OI + bi * 64, umma_smem_desc(smem_u32(Ps) + kk * 32, 16, 1024),
                               umma_smem_desc(smem_u32(VT) + kk * 32, 16, 1024), IDESC_OI, kk > 0);
                 umma_commit(&bar_o[bi]);
-                // OX_c = Q_c S^T once the back wrote the bf16 state after chunk c-1
+                umma_commit(&empty[st]);   // K_c no longer read once these complete
+            }
+            // nothing of this block's may still run on the tensor cores when
+            // its TMEM is released
+            umma_commit(mma_done);
+            mbar_wait_bounded(mma_done, 0, timeout_ns);
+        }
+    } else if (warp == OX_WARP) {  // -------------------------------------- OX
+        if (lane == 0) {
+            for (int c = 0; c < n_chunks; ++c) {
+                const int st = c % NST, bi = c & 1;
+                // the bf16 state after chunk c-1, Q_c, and the OX buffer of
+                // chunk c-2 released by the back
                 if (!hw(sbready, c & 1)) break;
+                if (!hw(&full[st], (c / NST) & 1)) break;
+                if (c >= 2 && !hw(&kdone[bi], ((c - 2) >> 1) & 1)) break;
                 tc_fence_after();
+                const uint32_t sQ = smem_u32(sm + st * STAGE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t qoff = (kk >> 2) * 8192 + (kk & 3) * 32;
@@ -276,10 +294,8 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                               umma_smem_desc(smem_u32(SBT) + kk * 2048, 8192, 1024), IDESC_OX, kk > 0);
                 }
                 umma_commit(&bar_x[bi]);
-                umma_commit(&empty[st]);   // Q_c, K_c are no longer read once these complete
+                umma_commit(&empty[st]);   // Q_c no longer read once these complete
             }
-            // nothing of this block's may still run on the tensor cores when
-            // its TMEM is released
             umma_commit(mma_done);
             mbar_wait_bounded(mma_done, 0, timeout_ns);
         }
