@@ -194,13 +194,51 @@ def _back(out: torch.Tensor, host: bool) -> torch.Tensor:
     return h
 
 
+def _outputs(out, specs, dev):
+    """Device buffers the kernel writes, and the caller's host destinations.
+
+    ``out`` is None or a tuple of tensors matching ``specs`` (shape, dtype):
+    all on the GPU (the kernel writes them in place) or all on the host
+    (results are copied into them; pinned memory keeps the copy
+    asynchronous and avoids allocating a pinned buffer per call)."""
+    if out is None:
+        return [torch.empty(sh, dtype=dt, device=dev) for sh, dt in specs], None
+    if len(out) != len(specs):
+        raise ValueError(f"out must hold {len(specs)} tensors")
+    for o, (sh, dt) in zip(out, specs):
+        if tuple(o.shape) != tuple(sh) or o.dtype != dt or not o.is_contiguous():
+            raise ValueError(f"out tensor {tuple(o.shape)} {o.dtype} does not match "
+                             f"{tuple(sh)} {dt} (contiguous)")
+    on_gpu = [o.device.type == "cuda" for o in out]
+    if all(on_gpu):
+        if any(o.device != dev for o in out):
+            raise ValueError("out tensors must be on the inputs' GPU")
+        return list(out), None
+    if any(on_gpu):
+        raise ValueError("out tensors must be all on the GPU or all on the host")
+    return [torch.empty(sh, dtype=dt, device=dev) for sh, dt in specs], list(out)
+
+
+def _finish(bufs, host_out, host: bool, dev, sync_host: bool):
+    if host_out is not None:
+        for dst, src in zip(host_out, bufs):
+            dst.copy_(src, non_blocking=True)
+        res = host_out
+    else:
+        res = [_back(b, host) for b in bufs]
+    if (host or host_out is not None) and sync_host:
+        torch.cuda.current_stream(dev).synchronize()
+    return tuple(res)
+
+
 def selective_scan(x, dt, Bm, Cm, A_log, z=None, Dskip=None, h0=None,
-                   dt_softplus: bool = True, workspace=None,
+                   dt_softplus: bool = True, workspace=None, out=None,
                    sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """Selective SSM scan.  x, dt, z: (B, L, D); Bm, Cm: (B, L, 16), all one
     dtype (float32 or bfloat16); A_log: (D, 16) fp32; Dskip: (D,) fp32;
     h0: (B, D, 16) fp32.  Returns (y (B, L, D) in the I/O dtype, h_final
-    (B, D, 16) fp32).  Host inputs are copied to the GPU and results back."""
+    (B, D, 16) fp32).  Host inputs are copied to the GPU and results back;
+    ``out=(y, h_final)`` gives the result tensors (GPU or host)."""
     host = x.device.type != "cuda"
     dev = _target_device(x)
     x, dt, z, Bm, Cm = (_dev(t, dev) for t in (x, dt, z, Bm, Cm))
@@ -209,25 +247,21 @@ def selective_scan(x, dt, Bm, Cm, A_log, z=None, Dskip=None, h0=None,
     io = _io_of(x)
     B, L, D = x.shape
     N = Bm.shape[-1]
-    y = torch.empty_like(x)
-    hf = torch.empty(B, D, N, dtype=torch.float32, device=dev)
+    (y, hf), host_out = _outputs(out, [((B, L, D), x.dtype), ((B, D, N), torch.float32)], dev)
     ws, wsb = _workspace(lr_selective_scan_workspace_size(B, L, D, N, io), dev, workspace)
     stream = torch.cuda.current_stream(dev).cuda_stream
     _check(lr_selective_scan_fwd(_ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm),
                                  _ptr(A_log), _ptr(Dskip), _ptr(h0), _ptr(y),
                                  _ptr(hf), B, L, D, N, io, int(bool(dt_softplus)),
                                  _ptr(ws), wsb, stream), "lr_selective_scan_fwd")
-    y, hf = _back(y, host), _back(hf, host)
-    if host and sync_host:
-        torch.cuda.current_stream(dev).synchronize()
-    return y, hf
+    return _finish((y, hf), host_out, host, dev, sync_host)
 
 
-def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None,
+def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None, out=None,
                sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """RG-LRU scan.  x, r, i: (B, L, D) (r, i after their sigmoid), one dtype;
     a_log: (D,) fp32; h0: (B, D) fp32.  Returns (y (B, L, D), h_final (B, D)
-    fp32)."""
+    fp32); ``out=(y, h_final)`` gives the result tensors (GPU or host)."""
     host = x.device.type != "cuda"
     dev = _target_device(x)
     x, r, i = (_dev(t, dev) for t in (x, r, i))
@@ -235,24 +269,21 @@ def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None,
     _same(x, r, i)
     io = _io_of(x)
     B, L, D = x.shape
-    y = torch.empty_like(x)
-    hf = torch.empty(B, D, dtype=torch.float32, device=dev)
+    (y, hf), host_out = _outputs(out, [((B, L, D), x.dtype), ((B, D), torch.float32)], dev)
     ws, wsb = _workspace(lr_rglru_scan_workspace_size(B, L, D, io), dev, workspace)
     stream = torch.cuda.current_stream(dev).cuda_stream
     _check(lr_rglru_scan_fwd(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c),
                              _ptr(h0), _ptr(y), _ptr(hf), B, L, D, io, _ptr(ws),
                              wsb, stream), "lr_rglru_scan_fwd")
-    y, hf = _back(y, host), _back(hf, host)
-    if host and sync_host:
-        torch.cuda.current_stream(dev).synchronize()
-    return y, hf
+    return _finish((y, hf), host_out, host, dev, sync_host)
 
 
-def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None,
+def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None,
           sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
     """HGRN2 matrix-state recurrence.  q, k: (B, L, H*dk); v, g: (B, L, H*dv)
     (g after its activation and lower bound), bfloat16; S0: (B, H, dv, dk)
-    fp32.  Returns (o (B, L, H*dv), S_final (B, H, dv, dk) fp32).  Raises
+    fp32.  Returns (o (B, L, H*dv), S_final (B, H, dv, dk) fp32);
+    ``out=(o, S_final)`` gives the result tensors (GPU or host).  Raises
     ValueError when the hidden size is not divisible by the head count."""
     if q.shape[-1] % H or v.shape[-1] % H:
         raise ValueError(f"hidden size {q.shape[-1]} is not divisible by {H} heads")
@@ -264,17 +295,14 @@ def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None,
     io = _io_of(q)
     B, L, HK = q.shape
     dk, dv = HK // H, v.shape[-1] // H
-    o = torch.empty(B, L, H * dv, dtype=q.dtype, device=dev)
-    Sf = torch.empty(B, H, dv, dk, dtype=torch.float32, device=dev)
+    (o, Sf), host_out = _outputs(out, [((B, L, H * dv), q.dtype), ((B, H, dv, dk), torch.float32)],
+                                 dev)
     ws, wsb = _workspace(lr_hgrn2_workspace_size(B, L, H, dk, dv, io), dev, workspace)
     stream = torch.cuda.current_stream(dev).cuda_stream
     _check(lr_hgrn2_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0), _ptr(o),
                         _ptr(Sf), B, L, H, dk, dv, chunk, io, _ptr(ws), wsb,
                         stream), "lr_hgrn2_fwd")
-    o, Sf = _back(o, host), _back(Sf, host)
-    if host and sync_host:
-        torch.cuda.current_stream(dev).synchronize()
-    return o, Sf
+    return _finish((o, Sf), host_out, host, dev, sync_host)
 
 
 def check_status(stream=None) -> None:
