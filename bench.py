@@ -274,6 +274,59 @@ def make_call(lr, cfg, p, out=None):
     return lambda: lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=p["H"], out=out)
 
 
+def decode_timings(lr, cfgs, dev, steps: int = 20, reps: int = 20) -> list:
+    """Single-token decode: `steps` in-place steps of each form at the
+    workload's batch and width, captured in one CUDA graph and replayed;
+    per-step device time and the bytes a step must move (state read and
+    written, inputs read, output written)."""
+    res = []
+    for cfg in cfgs:
+        p = wl.make_inputs(cfg, device=dev, L=1)
+        es = 2 if cfg.io == "bf16" else 4
+        if cfg.form == "rglru":
+            h = torch.zeros(cfg.B, cfg.D, device=dev)
+            args = [p[n][:, 0].contiguous() for n in ("x", "r", "i")]
+            fn = lambda: lr.rglru_scan_step(*args, p["a_log"], p["c"], h=h, h_out=h)
+            by = 8 * cfg.B * cfg.D + 4 * es * cfg.B * cfg.D + 4 * cfg.D
+        elif cfg.form == "selective":
+            h = torch.zeros(cfg.B, cfg.D, cfg.N, device=dev)
+            args = [p[n][:, 0].contiguous() for n in ("x", "dt", "Bm", "Cm")]
+            zt = p["z"][:, 0].contiguous()
+            fn = lambda: lr.selective_scan_step(*args, p["A_log"], z=zt, Dskip=p["Dskip"], h=h, h_out=h)
+            by = (8 * cfg.B * cfg.D * cfg.N + 4 * es * cfg.B * cfg.D + 2 * es * cfg.B * cfg.N
+                  + 4 * cfg.D * (cfg.N + 1))
+        else:
+            d = cfg.head_dim
+            h = torch.zeros(cfg.B, cfg.H, d, d, device=dev)
+            args = [p[n][:, 0].contiguous() for n in ("q", "k", "v", "g")]
+            fn = lambda: lr.hgrn2_step(*args, cfg.H, S=h, S_out=h)
+            by = 8 * cfg.B * cfg.H * d * d + 5 * es * cfg.B * cfg.H * d
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream(dev)
+        with torch.cuda.stream(st):
+            fn()
+            st.synchronize()
+            with torch.cuda.graph(g, stream=st):
+                for _ in range(steps):
+                    fn()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
+        res.append({"workload": f"{cfg.form} step B={cfg.B}" +
+                    (f" H={cfg.H} d={cfg.head_dim}" if cfg.form == "hgrn2" else f" D={cfg.D}"),
+                    "us_per_step": us, "bytes_per_step": by, "gb_per_s": by / (us * 1e-6) / 1e9})
+    return res
+
+
 def input_bytes(p) -> int:
     return sum(t.numel() * t.element_size() for t in p.values() if torch.is_tensor(t))
 
@@ -382,6 +435,8 @@ def gpu_arm(args):
         "gpu_launches": len(cfgs) * args.steps,
         "clocks": clk,
     }
+    if not args.seq_len:
+        line["decode"] = decode_timings(lr, cfgs, dev)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfgs)
     if rank == 0:

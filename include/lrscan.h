@@ -209,6 +209,47 @@ int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g,
                  void *workspace, size_t ws_bytes, lr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Single-token decode steps                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One step (L = 1) of each recurrence with a carried state, as the pages run
+ * their layers token by token:
+ *   [SSM] MultiScaleSSM.forward with past_state and one token,
+ *   [RGLRU] RGLRU.step, [HGRN2] the per-token update S = diag(g) S + v k^T.
+ * The arithmetic is that of the matching *_fwd call with L = 1 (same inputs,
+ * same readout after the update); the kernels use the accurate math library
+ * functions.  The state before the step (h_in / S_in) may be NULL for a zero
+ * state; the state after it (h_out / S_out) is always written and may be the
+ * same buffer as h_in / S_in (in-place update).  No workspace.  Shapes:
+ *   selective: x, dt, z, y: (B, D) io; Bm, Cm: (B, N) io; A_log: (D, N) fp32;
+ *              Dskip: (D) fp32 or NULL; z NULL = no gate; h_in, h_out:
+ *              (B, D, N) fp32.  N must be 16.
+ *   rglru:     x, r, i, y: (B, D) io; a_log: (D) fp32; h_in, h_out: (B, D)
+ *              fp32.
+ *   hgrn2:     q, k: (B, H*dk) io; v, g, o: (B, H*dv) io; S_in, S_out:
+ *              (B, H, dv, dk) fp32.  Any dk, dv >= 1 and either io dtype.
+ * Errors: LR_ERR_INVALID_ARG for a NULL required pointer or a negative size,
+ * LR_ERR_UNSUPPORTED for N != 16, LR_ERR_MISALIGNED as for every call.
+ */
+int lr_selective_scan_step(const void *x, const void *dt, const void *z,
+                           const void *Bm, const void *Cm,
+                           const float *A_log, const float *Dskip,
+                           const float *h_in, float *h_out, void *y,
+                           int64_t B, int64_t D, int64_t N, lr_dtype io,
+                           int dt_softplus, lr_stream_t stream);
+
+int lr_rglru_scan_step(const void *x, const void *r, const void *i,
+                       const float *a_log, float c, const float *h_in,
+                       float *h_out, void *y, int64_t B, int64_t D,
+                       lr_dtype io, lr_stream_t stream);
+
+int lr_hgrn2_step(const void *q, const void *k, const void *v, const void *g,
+                  const float *S_in, float *S_out, void *o,
+                  int64_t B, int64_t H, int64_t dk, int64_t dv, lr_dtype io,
+                  lr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Tuning and test hooks                                                     */
 /* ------------------------------------------------------------------------ */
 

@@ -49,6 +49,10 @@ SIGNATURES = {
     "lr_hgrn2_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I]),
     "lr_hgrn2_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                           _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_selective_scan_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _I64, _I64, _I64, _I, _I, _P]),
+    "lr_rglru_scan_step": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _I64, _I64, _I, _P]),
+    "lr_hgrn2_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _P]),
 }
 
 
@@ -137,6 +141,22 @@ def lr_hgrn2_fwd(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io,
                  workspace, ws_bytes, stream) -> int:
     return int(_lib.lr_hgrn2_fwd(q, k, v, g, S0, o, S_final, B, L, H, dk, dv,
                                  chunk, io, workspace, ws_bytes, stream))
+
+
+def lr_selective_scan_step(x, dt, z, Bm, Cm, A_log, Dskip, h_in, h_out, y, B, D, N,
+                           io, dt_softplus, stream) -> int:
+    return int(_lib.lr_selective_scan_step(x, dt, z, Bm, Cm, A_log, Dskip, h_in, h_out,
+                                           y, B, D, N, io, dt_softplus, stream))
+
+
+def lr_rglru_scan_step(x, r, i, a_log, c, h_in, h_out, y, B, D, io, stream) -> int:
+    return int(_lib.lr_rglru_scan_step(x, r, i, a_log, c, h_in, h_out, y, B, D, io,
+                                       stream))
+
+
+def lr_hgrn2_step(q, k, v, g, S_in, S_out, o, B, H, dk, dv, io, stream) -> int:
+    return int(_lib.lr_hgrn2_step(q, k, v, g, S_in, S_out, o, B, H, dk, dv, io,
+                                  stream))
 
 
 # ------------------------------------------------------------ torch helpers
@@ -303,6 +323,73 @@ def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None
                         _ptr(Sf), B, L, H, dk, dv, chunk, io, _ptr(ws), wsb,
                         stream), "lr_hgrn2_fwd")
     return _finish((o, Sf), host_out, host, dev, sync_host)
+
+
+def _step_state(state, shape, dev, state_out):
+    """(state before the step or None, state buffer the step writes)."""
+    h_in = None if state is None else _dev(state.float(), dev)
+    if state_out is None:
+        state_out = torch.empty(shape, dtype=torch.float32, device=dev)
+    elif (tuple(state_out.shape) != tuple(shape) or state_out.dtype != torch.float32
+          or state_out.device != dev or not state_out.is_contiguous()):
+        raise ValueError(f"state_out must be a contiguous fp32 GPU tensor of shape {tuple(shape)}")
+    return h_in, state_out
+
+
+def selective_scan_step(x, dt, Bm, Cm, A_log, z=None, Dskip=None, h=None,
+                        dt_softplus: bool = True, h_out=None):
+    """One decode step of the selective SSM.  x, dt, z: (B, D); Bm, Cm: (B, 16),
+    one dtype on the GPU; A_log: (D, 16); Dskip: (D,); h: (B, D, 16) fp32 or
+    None (zero).  Returns (y (B, D), h_new (B, D, 16) fp32); ``h_out`` gives
+    the buffer h_new is written to (it may be ``h`` itself)."""
+    dev = _target_device(x)
+    x, dt, z, Bm, Cm = (_dev(t, dev) for t in (x, dt, z, Bm, Cm))
+    A_log, Dskip = (_dev(None if t is None else t.float(), dev) for t in (A_log, Dskip))
+    _same(x, dt, z, Bm, Cm)
+    B, D = x.shape
+    N = Bm.shape[-1]
+    h_in, h_new = _step_state(h, (B, D, N), dev, h_out)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(lr_selective_scan_step(_ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _ptr(A_log),
+                                  _ptr(Dskip), _ptr(h_in), _ptr(h_new), _ptr(y), B, D, N,
+                                  _io_of(x), int(bool(dt_softplus)), stream),
+           "lr_selective_scan_step")
+    return y, h_new
+
+
+def rglru_scan_step(x, r, i, a_log, c: float = 8.0, h=None, h_out=None):
+    """One decode step of the RG-LRU.  x, r, i: (B, D) on the GPU; a_log: (D,);
+    h: (B, D) fp32 or None.  Returns (y (B, D), h_new (B, D) fp32)."""
+    dev = _target_device(x)
+    x, r, i = (_dev(t, dev) for t in (x, r, i))
+    a_log = _dev(a_log.float(), dev)
+    _same(x, r, i)
+    B, D = x.shape
+    h_in, h_new = _step_state(h, (B, D), dev, h_out)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(lr_rglru_scan_step(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c), _ptr(h_in),
+                              _ptr(h_new), _ptr(y), B, D, _io_of(x), stream), "lr_rglru_scan_step")
+    return y, h_new
+
+
+def hgrn2_step(q, k, v, g, H: int, S=None, S_out=None):
+    """One decode step of HGRN2.  q, k: (B, H*dk); v, g: (B, H*dv) on the GPU;
+    S: (B, H, dv, dk) fp32 or None.  Returns (o (B, H*dv), S_new)."""
+    if q.shape[-1] % H or v.shape[-1] % H:
+        raise ValueError(f"hidden size {q.shape[-1]} is not divisible by {H} heads")
+    dev = _target_device(q)
+    q, k, v, g = (_dev(t, dev) for t in (q, k, v, g))
+    _same(q, k, v, g)
+    B = q.shape[0]
+    dk, dv = q.shape[-1] // H, v.shape[-1] // H
+    S_in, S_new = _step_state(S, (B, H, dv, dk), dev, S_out)
+    o = torch.empty(B, H * dv, dtype=q.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(lr_hgrn2_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S_in), _ptr(S_new), _ptr(o),
+                         B, H, dk, dv, _io_of(q), stream), "lr_hgrn2_step")
+    return o, S_new
 
 
 def check_status(stream=None) -> None:

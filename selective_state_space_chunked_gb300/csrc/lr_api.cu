@@ -90,6 +90,16 @@ int validate_hgrn2(const void *q, const void *k, const void *v, const void *g, c
     return LR_OK;
 }
 
+// Decode steps: the state after the step is always written (h_out
+// required); the state before it is optional (NULL = zero).
+int validate_step_common(const void *const *required, int n_required, const void *const *all, int n_all) {
+    for (int k = 0; k < n_required; ++k)
+        if (required[k] == nullptr) return LR_ERR_INVALID_ARG;
+    for (int k = 0; k < n_all; ++k)
+        if (misaligned(all[k])) return LR_ERR_MISALIGNED;
+    return LR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -226,3 +236,48 @@ int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g, con
 }
 
 }  // extern "C"
+
+extern "C" int lr_selective_scan_step(const void *x, const void *dt, const void *z, const void *Bm,
+                                      const void *Cm, const float *A_log, const float *Dskip,
+                                      const float *h_in, float *h_out, void *y, int64_t B, int64_t D,
+                                      int64_t N, lr_dtype io, int dt_softplus, lr_stream_t stream) {
+    if (B < 0 || D < 0 || N < 0 || !io_ok(io)) return LR_ERR_INVALID_ARG;
+    if (N != 16) return LR_ERR_UNSUPPORTED;
+    if (B * D > 0) {
+        const void *req[] = {x, dt, Bm, Cm, A_log, h_out, y};
+        const void *all[] = {x, dt, z, Bm, Cm, A_log, Dskip, h_in, h_out, y};
+        const int rc = validate_step_common(req, 7, all, 10);
+        if (rc != LR_OK) return rc;
+    }
+    return lr::selective_step_launch(x, dt, z, Bm, Cm, A_log, Dskip, h_in, h_out, y, B, D, io == LR_BF16,
+                                     dt_softplus, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int lr_rglru_scan_step(const void *x, const void *r, const void *i, const float *a_log,
+                                  float c, const float *h_in, float *h_out, void *y, int64_t B,
+                                  int64_t D, lr_dtype io, lr_stream_t stream) {
+    if (B < 0 || D < 0 || !io_ok(io) || !std::isfinite(c)) return LR_ERR_INVALID_ARG;
+    if (B * D > 0) {
+        const void *req[] = {x, r, i, a_log, h_out, y};
+        const void *all[] = {x, r, i, a_log, h_in, h_out, y};
+        const int rc = validate_step_common(req, 6, all, 7);
+        if (rc != LR_OK) return rc;
+    }
+    return lr::rglru_step_launch(x, r, i, a_log, c, h_in, h_out, y, B, D, io == LR_BF16,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int lr_hgrn2_step(const void *q, const void *k, const void *v, const void *g,
+                             const float *S_in, float *S_out, void *o, int64_t B, int64_t H,
+                             int64_t dk, int64_t dv, lr_dtype io, lr_stream_t stream) {
+    if (B < 0 || H <= 0 || dk <= 0 || dv <= 0 || !io_ok(io)) return LR_ERR_INVALID_ARG;
+    if (B > 0) {
+        const void *req[] = {q, k, v, g, S_out, o};
+        const void *all[] = {q, k, v, g, S_in, S_out, o};
+        const int rc = validate_step_common(req, 6, all, 7);
+        if (rc != LR_OK) return rc;
+    }
+    return lr::hgrn2_step_launch(q, k, v, g, S_in, S_out, o, B, H, dk, dv, io == LR_BF16,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+

@@ -150,3 +150,60 @@ def test_package_has_no_cpu_fallback():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+# ----------------------------------------------------------- decode steps
+def call_sel_step(lr, **kw):
+    a = dict(x=FAKE, dt=FAKE, z=FAKE, Bm=FAKE, Cm=FAKE, A_log=FAKE, Dskip=FAKE,
+             h_in=FAKE, h_out=FAKE, y=FAKE, B=2, D=64, N=16, io=1, dt_softplus=1,
+             stream=None)
+    a.update(kw)
+    return lr.lr_selective_scan_step(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), -1), (dict(Bm=None), -1), (dict(A_log=None), -1), (dict(h_out=None), -1),
+    (dict(y=None), -1), (dict(B=-1), -1), (dict(io=3), -1),
+    (dict(N=8), -2),
+    (dict(h_in=FAKE + 4), -3), (dict(y=FAKE + 2), -3),
+])
+def test_selective_step_validation_codes(lr, kw, code):
+    assert call_sel_step(lr, **kw) == code
+
+
+def call_rg_step(lr, **kw):
+    a = dict(x=FAKE, r=FAKE, i=FAKE, a_log=FAKE, c=8.0, h_in=FAKE, h_out=FAKE, y=FAKE,
+             B=2, D=64, io=1, stream=None)
+    a.update(kw)
+    return lr.lr_rglru_scan_step(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(r=None), -1), (dict(h_out=None), -1), (dict(c=float("nan")), -1), (dict(D=-1), -1),
+    (dict(i=FAKE + 8), -3),
+])
+def test_rglru_step_validation_codes(lr, kw, code):
+    assert call_rg_step(lr, **kw) == code
+
+
+def call_hg_step(lr, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, S_in=FAKE, S_out=FAKE, o=FAKE, B=2, H=4,
+             dk=128, dv=128, io=1, stream=None)
+    a.update(kw)
+    return lr.lr_hgrn2_step(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(v=None), -1), (dict(S_out=None), -1), (dict(H=0), -1), (dict(dk=0), -1),
+    (dict(B=-1), -1), (dict(io=5), -1),
+    (dict(S_in=FAKE + 4), -3),
+])
+def test_hgrn2_step_validation_codes(lr, kw, code):
+    assert call_hg_step(lr, **kw) == code
+
+
+def test_steps_with_no_elements_launch_nothing(lr):
+    # zero batch: nothing to do, no pointer needed, no CUDA call made
+    assert call_sel_step(lr, B=0, x=None, y=None, h_out=None) == 0
+    assert call_rg_step(lr, D=0, x=None, y=None, h_out=None) == 0
+    assert call_hg_step(lr, B=0, q=None, o=None, S_out=None) == 0

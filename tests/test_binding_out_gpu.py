@@ -32,7 +32,17 @@ def calls(lr):
     ]
 
 
-def test_out_on_gpu_and_host_match_default(lr):
+@pytest.fixture
+def one_split(lr):
+    # A single time split keeps the diagonal scans bit-reproducible: with
+    # several, the look-back may combine carries in a different rounding
+    # order from one run to the next.
+    lr.lr_set_split_override(1)
+    yield
+    lr.lr_set_split_override(0)
+
+
+def test_out_on_gpu_and_host_match_default(lr, one_split):
     for p, fn in calls(lr):
         dp = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in p.items()}
         ref = [t.cpu() for t in fn(dp, None)]
