@@ -17,8 +17,10 @@ Functions (sources are cited in ``lro_oracle.c``):
 * :func:`rglru_scan`      -- lrnnx ``RGLRU.step`` fallback update, every step.
 * :func:`hgrn2`           -- HGRN2 Attention ``S_t = diag(g_t) S_{t-1} + v_t k_t^T``
   with the readout ``o_t = S_t q_t``.
+* :func:`minmax_scan`     -- minmaxrnc ``MinMaxNeuron`` recurrence
+  ``x_t = max(min(r_t, x_{t-1}), s_t)``, every state returned.
 
-All three are pinned against closed forms, brute force and library routines
+All four are pinned against closed forms, brute force and library routines
 in ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
@@ -87,6 +89,9 @@ def _load():
                 dp, dp, dp, dp, dp, i64, i64, i64, i64, i64, dp, dp,
                 ctypes.c_int]
             lib.lro_hgrn2_ref.restype = ctypes.c_int
+            lib.lro_minmax_scan_ref.argtypes = [
+                dp, dp, dp, i64, i64, i64, dp, dp, ctypes.c_int]
+            lib.lro_minmax_scan_ref.restype = ctypes.c_int
             lib.lro_max_threads.argtypes = []
             lib.lro_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -183,3 +188,22 @@ def hgrn2(q, k, v, g, H, S0=None, threads=0):
     if rc != 0:
         raise ValueError("lro_hgrn2_ref rejected its arguments")
     return o, Sf
+
+
+def minmax_scan(r, s, x0=None, threads=0):
+    """MinMax recurrence x_t = max(min(r_t, x_{t-1}), s_t) in float64.
+
+    r, s: (B, L, D); x0: (B, D) (zero when None).  Returns
+    ``(y (B, L, D) = the states after every step, x_final (B, D))``.
+    """
+    r, s = map(_f64, (r, s))
+    x0 = _f64(x0)
+    Bsz, L, D = r.shape
+    assert s.shape == r.shape and (x0 is None or x0.shape == (Bsz, D))
+    y = np.zeros((Bsz, L, D), dtype=np.float64)
+    xf = np.zeros((Bsz, D), dtype=np.float64)
+    rc = _load().lro_minmax_scan_ref(_ptr(r), _ptr(s), _ptr(x0), Bsz, L, D, _ptr(y), _ptr(xf),
+                                     int(threads))
+    if rc != 0:
+        raise ValueError("lro_minmax_scan_ref rejected its arguments")
+    return y, xf

@@ -24,9 +24,13 @@
  *   [HGRN2] frankenstein-transformer API docs, HGRN2 Attention page: the
  *           state update S_t = diag(g_t) S_{t-1} + v_t k_t^T and the
  *           token-by-token forward description.
+ *   [MINMAX] minmaxrnc 0.1.0 wheel: minmax_neuron.py (MinMaxNeuron class
+ *           docstring, x_{t+1} = max(min(r_t, x_t), s_t); forward, which
+ *           returns the states after every step and the last state) and
+ *           minmax_operator.py (apply: f(x) = max(min(a, x), b)).
  *
  * Parity pins (closed forms, brute force, library special cases) live in
- * tests/test_oracle_pins.py.  All three functions are pinned there.
+ * tests/test_oracle_pins.py.  All four functions are pinned there.
  *
  * Layouts (row-major, contiguous):
  *   selective: x, dt, z, y: (B, L, D); Bm, Cm: (B, L, N); A_log: (D, N);
@@ -35,6 +39,7 @@
  *   hgrn2:     q, k: (B, L, H*dk); v, g, o: (B, L, H*dv);
  *              S0, S_final: (B, H, dv, dk)   (row i = value channel,
  *              column j = key channel)
+ *   minmax:    r, s, y: (B, L, D); x0, x_final: (B, D)
  *
  * Return value: 0 on success, -1 on an invalid argument (nothing written).
  */
@@ -232,4 +237,42 @@ int lro_hgrn2_ref(const double *q, const double *k, const double *v,
         free(S);
     }
     return failed ? -1 : 0;
+}
+
+/*
+ * MinMax recurrence, [MINMAX] MinMaxNeuron, one step at a time.  For each
+ * (b, d):
+ *
+ *   x = x0[b,d]  (zero when x0 == NULL: the neuron's default initial state)
+ *   for t in 0..L-1:
+ *     x = max(min(r[b,t,d], x), s[b,t,d])   (the operator f(x) = max(min(a, x), b)
+ *                                           with a = r_t, b = s_t)
+ *     y[b,t,d] = x                          (forward returns the states after
+ *                                           every step)
+ *   x_final[b,d] = x
+ *
+ * fmin / fmax of two non-NaN doubles return one of them exactly, so the
+ * result is exact: every output equals one of the inputs or x0.
+ */
+int lro_minmax_scan_ref(const double *r, const double *s, const double *x0,
+                        int64_t B, int64_t L, int64_t D,
+                        double *y, double *x_final, int nthreads)
+{
+    if (!r || !s || !y) return -1;
+    if (B < 0 || L < 0 || D < 0) return -1;
+    set_threads(nthreads);
+    int64_t bd;
+#pragma omp parallel for schedule(static)
+    for (bd = 0; bd < B * D; ++bd) {
+        const int64_t b = bd / D, d = bd % D;
+        double x = x0 ? x0[b * D + d] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            const int64_t i = (b * L + t) * D + d;
+            const double lo = r[i] < x ? r[i] : x;      /* min(r_t, x) */
+            x = lo > s[i] ? lo : s[i];                  /* max(., s_t) */
+            y[i] = x;
+        }
+        if (x_final) x_final[b * D + d] = x;
+    }
+    return 0;
 }

@@ -429,3 +429,95 @@ def test_hgrn2_workload_gate_bounds():
     gv = p["g"].float()
     assert float(gv.min()) >= 0.2 - 1e-3 and float(gv.max()) <= 1.0
     assert p["q"].dtype == torch.bfloat16
+
+
+# ------------------------------------------------------------------ MinMax
+# [MINMAX] minmaxrnc minmax_neuron.py (MinMaxNeuron: x_{t+1} = max(min(r_t,
+# x_t), s_t), forward returns every state) and minmax_operator.py (apply,
+# compose).
+def minmax_inputs(B, L, D, seed, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    r = torch.randn(B, L, D, generator=g).to(dtype)
+    s = torch.randn(B, L, D, generator=g).to(dtype) - 1.0
+    x0 = torch.randn(B, D, generator=g).to(dtype).float()
+    return r, s, x0
+
+
+def test_minmax_identity_operators_keep_the_state():
+    """a = +inf, b = -inf is the identity operator of minmax_operator.apply."""
+    B, L, D = 2, 9, 5
+    _, _, x0 = minmax_inputs(B, L, D, 1)
+    r = np.full((B, L, D), np.inf)
+    s = np.full((B, L, D), -np.inf)
+    y, xf = oracle.minmax_scan(r, s, x0)
+    assert np.array_equal(y, np.broadcast_to(x0.numpy()[:, None, :], (B, L, D)))
+    assert np.array_equal(xf, x0.numpy())
+
+
+def test_minmax_without_upper_bound_is_a_running_max():
+    """r = +inf: x_t = max(x_{t-1}, s_t), numpy's running maximum."""
+    B, L, D = 3, 40, 7
+    _, s, x0 = minmax_inputs(B, L, D, 2)
+    y, xf = oracle.minmax_scan(np.full((B, L, D), np.inf), s, x0)
+    seq = np.concatenate([x0.numpy()[:, None, :], s.numpy().astype(np.float64)], axis=1)
+    ref = np.maximum.accumulate(seq, axis=1)[:, 1:, :]
+    assert np.array_equal(y, ref) and np.array_equal(xf, ref[:, -1])
+
+
+def test_minmax_without_lower_bound_is_a_running_min():
+    """s = -inf: x_t = min(r_t, x_{t-1}), numpy's running minimum."""
+    B, L, D = 3, 40, 7
+    r, _, x0 = minmax_inputs(B, L, D, 3)
+    y, _ = oracle.minmax_scan(r, np.full((B, L, D), -np.inf), x0)
+    seq = np.concatenate([x0.numpy()[:, None, :], r.numpy().astype(np.float64)], axis=1)
+    assert np.array_equal(y, np.minimum.accumulate(seq, axis=1)[:, 1:, :])
+
+
+def _compose(a2, b2, a1, b1):
+    # minmax_operator.compose: f2(f1(x)) = max(min(min(a2, a1), x), max(min(a2, b1), b2))
+    return np.minimum(a2, a1), np.maximum(np.minimum(a2, b1), b2)
+
+
+def test_minmax_states_equal_the_composed_operator_applied_to_x0():
+    """Every state equals the page's closed-form composition of the first t
+    operators applied once to x0 (a different computation from the loop)."""
+    B, L, D = 2, 33, 6
+    r, s, x0 = minmax_inputs(B, L, D, 4)
+    r64, s64, x64 = r.numpy().astype(np.float64), s.numpy().astype(np.float64), x0.numpy()
+    y, _ = oracle.minmax_scan(r, s, x0)
+    a = np.full((B, D), np.inf)
+    b = np.full((B, D), -np.inf)
+    for t in range(L):
+        a, b = _compose(r64[:, t], s64[:, t], a, b)
+        assert np.array_equal(y[:, t], np.maximum(np.minimum(a, x64), b))
+
+
+def test_minmax_outputs_are_inputs_and_respect_the_bounds():
+    B, L, D = 2, 50, 8
+    r, s, x0 = minmax_inputs(B, L, D, 5, torch.bfloat16)
+    y, _ = oracle.minmax_scan(r, s, x0)
+    r64, s64 = r.double().numpy(), s.double().numpy()
+    assert np.all(y >= s64) and np.all(y <= np.maximum(r64, s64))
+    pool = np.concatenate([x0.double().numpy()[:, None, :], r64, s64], axis=1)
+    for b_ in range(B):
+        for d in range(D):
+            assert set(y[b_, :, d]).issubset(set(pool[b_, :, d]))
+
+
+@pytest.mark.parametrize("segments", [2, 5])
+def test_minmax_split_resume_equals_full(segments):
+    B, L, D = 2, 60, 4
+    r, s, x0 = minmax_inputs(B, L, D, 6)
+    y, xf = oracle.minmax_scan(r, s, x0)
+    x = x0
+    ys = []
+    for seg in np.array_split(np.arange(L), segments):
+        yy, x = oracle.minmax_scan(r[:, seg], s[:, seg], x)
+        ys.append(yy)
+    assert np.array_equal(np.concatenate(ys, 1), y) and np.array_equal(x, xf)
+
+
+def test_minmax_zero_length_and_default_state():
+    r, s, _ = minmax_inputs(1, 0, 3, 7)
+    y, xf = oracle.minmax_scan(r, s)
+    assert y.shape == (1, 0, 3) and np.array_equal(xf, np.zeros((1, 3)))
