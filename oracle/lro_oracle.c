@@ -251,9 +251,13 @@ int lro_hgrn2_ref(const double *q, const double *k, const double *v,
  *                                           every step)
  *   x_final[b,d] = x
  *
- * fmin / fmax of two non-NaN doubles return one of them exactly, so the
- * result is exact: every output equals one of the inputs or x0.
+ * min and max return one of their arguments exactly, so the result is
+ * exact: every output equals one of the inputs or x0.  As torch.minimum and
+ * torch.maximum in the page's apply, a NaN argument gives NaN.
  */
+static double min_nan(double a, double b) { return isnan(a) || isnan(b) ? NAN : (a < b ? a : b); }
+static double max_nan(double a, double b) { return isnan(a) || isnan(b) ? NAN : (a > b ? a : b); }
+
 int lro_minmax_scan_ref(const double *r, const double *s, const double *x0,
                         int64_t B, int64_t L, int64_t D,
                         double *y, double *x_final, int nthreads)
@@ -268,8 +272,7 @@ int lro_minmax_scan_ref(const double *r, const double *s, const double *x0,
         double x = x0 ? x0[b * D + d] : 0.0;
         for (int64_t t = 0; t < L; ++t) {
             const int64_t i = (b * L + t) * D + d;
-            const double lo = r[i] < x ? r[i] : x;      /* min(r_t, x) */
-            x = lo > s[i] ? lo : s[i];                  /* max(., s_t) */
+            x = max_nan(min_nan(r[i], x), s[i]);
             y[i] = x;
         }
         if (x_final) x_final[b * D + d] = x;

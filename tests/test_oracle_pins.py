@@ -521,3 +521,22 @@ def test_minmax_zero_length_and_default_state():
     r, s, _ = minmax_inputs(1, 0, 3, 7)
     y, xf = oracle.minmax_scan(r, s)
     assert y.shape == (1, 0, 3) and np.array_equal(xf, np.zeros((1, 3)))
+
+
+def test_minmax_nan_propagates_like_the_page_operator():
+    """minmax_operator.apply uses torch.minimum / torch.maximum, which return
+    NaN when either argument is NaN: a NaN input poisons every later state."""
+    B, L, D = 1, 12, 4
+    r, s, x0 = minmax_inputs(B, L, D, 8)
+    r[0, 3, 1] = float("nan")
+    s[0, 7, 2] = float("nan")
+    y, xf = oracle.minmax_scan(r, s, x0)
+    x = x0.double()
+    ref = []
+    for t in range(L):
+        x = torch.maximum(torch.minimum(r[:, t].double(), x), s[:, t].double())
+        ref.append(x)
+    ref = torch.stack(ref, 1).numpy()
+    assert np.array_equal(np.isnan(y), np.isnan(ref))
+    assert np.array_equal(y[~np.isnan(y)], ref[~np.isnan(ref)])
+    assert np.isnan(y[0, 3:, 1]).all() and np.isnan(y[0, 7:, 2]).all()
