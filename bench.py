@@ -327,6 +327,35 @@ def decode_timings(lr, cfgs, dev, steps: int = 20, reps: int = 20) -> list:
     return res
 
 
+def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
+    """Scans outside the step, timed the same way (inputs larger than L2,
+    CUDA events on the launching stream): the MinMax recurrence at the
+    RG-LRU workload's shape, bf16 I/O."""
+    B, L, D = 8, 4096, 2560
+    g = torch.Generator(device=dev).manual_seed(11)
+    r = torch.randn(B, L, D, device=dev, generator=g).to(torch.bfloat16)
+    s_ = (torch.randn(B, L, D, device=dev, generator=g) - 1.0).to(torch.bfloat16)
+    x0 = torch.randn(B, D, device=dev, generator=g)
+    fn = lambda: lr.minmax_scan(r, s_, x0)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for a, b in ev:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    by = 3 * 2 * B * L * D + 2 * 4 * B * D
+    gbs = by / (ms * 1e-3) / 1e9
+    return [{"workload": f"minmax_bf16_B{B}_L{L}_D{D}", "ms": ms,
+             "tok_ch_per_s": B * L * D / (ms * 1e-3), "gb_per_s": gbs,
+             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}}]
+
+
 def input_bytes(p) -> int:
     return sum(t.numel() * t.element_size() for t in p.values() if torch.is_tensor(t))
 
@@ -435,8 +464,9 @@ def gpu_arm(args):
         "gpu_launches": len(cfgs) * args.steps,
         "clocks": clk,
     }
-    if not args.seq_len:
+    if not args.seq_len and not args.only:
         line["decode"] = decode_timings(lr, cfgs, dev)
+        line["extra"] = extra_timings(lr, dev, peaks)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfgs)
     if rank == 0:

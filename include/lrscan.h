@@ -18,6 +18,9 @@
  *   [HGRN2] frankenstein-transformer docs, HGRN2 Attention page --
  *           S_t = diag(g_t) S_{t-1} + v_t k_t^T, per-head matrix state,
  *           lower-bounded forget gate, hidden % heads check.
+ *   [MINMAX] minmaxrnc 0.1.0 wheel -- minmax_neuron.py (MinMaxNeuron:
+ *           x_{t+1} = max(min(r_t, x_t), s_t), forward returns every state
+ *           and the last one), minmax_operator.py (apply, compose).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -207,6 +210,34 @@ int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g,
                  int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
                  int64_t chunk, lr_dtype io,
                  void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* MinMax recurrence                                                         */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [MINMAX] MinMaxNeuron: for every batch row b and channel d,
+ *
+ *   x_t = max(min(r_t, x_{t-1}), s_t),   y_t = x_t   (the state after step t)
+ *
+ * with x_{-1} = x0[b,d] (zero when x0 == NULL, the neuron's default initial
+ * state) and x_final[b,d] = x after the last step.  r and s are the outputs
+ * of the neuron's two projections.  min and max select one argument, so the
+ * result is exact (every y equals an input or x0, rounded to `io` at the
+ * store only when x0 is not representable in it); a NaN argument gives NaN
+ * from then on, as torch.minimum / torch.maximum in the page's apply.
+ *
+ * Layouts: r, s, y: (B, L, D) in `io`; x0, x_final: (B, D) fp32.
+ * Optional: x0, x_final.
+ * Requirements: D % 8 == 0 for bf16, D % 4 == 0 for fp32 (LR_ERR_UNSUPPORTED).
+ * Workspace: as for the other diagonal scans (look-back scratch when the
+ * library splits time; query lr_minmax_scan_workspace_size).
+ */
+size_t lr_minmax_scan_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io);
+
+int lr_minmax_scan_fwd(const void *r, const void *s, const float *x0, void *y,
+                       float *x_final, int64_t B, int64_t L, int64_t D, lr_dtype io,
+                       void *workspace, size_t ws_bytes, lr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Single-token decode steps                                                 */

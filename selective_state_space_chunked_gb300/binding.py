@@ -49,6 +49,8 @@ SIGNATURES = {
     "lr_hgrn2_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I]),
     "lr_hgrn2_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                           _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_minmax_scan_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "lr_minmax_scan_fwd": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, _SZ, _P]),
     "lr_selective_scan_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _I64, _I64, _I64, _I, _I, _P]),
     "lr_rglru_scan_step": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _I64, _I64, _I, _P]),
@@ -141,6 +143,15 @@ def lr_hgrn2_fwd(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io,
                  workspace, ws_bytes, stream) -> int:
     return int(_lib.lr_hgrn2_fwd(q, k, v, g, S0, o, S_final, B, L, H, dk, dv,
                                  chunk, io, workspace, ws_bytes, stream))
+
+
+def lr_minmax_scan_workspace_size(B, L, D, io) -> int:
+    return int(_lib.lr_minmax_scan_workspace_size(B, L, D, io))
+
+
+def lr_minmax_scan_fwd(r, s, x0, y, x_final, B, L, D, io, workspace, ws_bytes, stream) -> int:
+    return int(_lib.lr_minmax_scan_fwd(r, s, x0, y, x_final, B, L, D, io, workspace, ws_bytes,
+                                       stream))
 
 
 def lr_selective_scan_step(x, dt, z, Bm, Cm, A_log, Dskip, h_in, h_out, y, B, D, N,
@@ -323,6 +334,27 @@ def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None
                         _ptr(Sf), B, L, H, dk, dv, chunk, io, _ptr(ws), wsb,
                         stream), "lr_hgrn2_fwd")
     return _finish((o, Sf), host_out, host, dev, sync_host)
+
+
+def minmax_scan(r, s, x0=None, workspace=None, out=None,
+                sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
+    """MinMax recurrence x_t = max(min(r_t, x_{t-1}), s_t).  r, s: (B, L, D),
+    one dtype (float32 or bfloat16); x0: (B, D) fp32 or None (zero).
+    Returns (y (B, L, D) = the state after every step, x_final (B, D) fp32);
+    ``out=(y, x_final)`` gives the result tensors (GPU or host)."""
+    host = r.device.type != "cuda"
+    dev = _target_device(r)
+    r, s = (_dev(t, dev) for t in (r, s))
+    x0 = _dev(None if x0 is None else x0.float(), dev)
+    _same(r, s)
+    io = _io_of(r)
+    B, L, D = r.shape
+    (y, xf), host_out = _outputs(out, [((B, L, D), r.dtype), ((B, D), torch.float32)], dev)
+    ws, wsb = _workspace(lr_minmax_scan_workspace_size(B, L, D, io), dev, workspace)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(lr_minmax_scan_fwd(_ptr(r), _ptr(s), _ptr(x0), _ptr(y), _ptr(xf), B, L, D, io, _ptr(ws),
+                              wsb, stream), "lr_minmax_scan_fwd")
+    return _finish((y, xf), host_out, host, dev, sync_host)
 
 
 def _step_state(state, shape, dev, state_out):

@@ -90,6 +90,18 @@ int validate_hgrn2(const void *q, const void *k, const void *v, const void *g, c
     return LR_OK;
 }
 
+int validate_minmax(const void *r, const void *s, const float *x0, const void *y, const float *x_final,
+                    int64_t B, int64_t L, int64_t D, lr_dtype io) {
+    if (B < 0 || L < 0 || D < 0 || !io_ok(io)) return LR_ERR_INVALID_ARG;
+    if (B > 0 && L > 0 && D > 0 && (!r || !s || !y)) return LR_ERR_INVALID_ARG;
+    if (!channels_ok(D, io)) return LR_ERR_UNSUPPORTED;
+    if (!fits_int(B) || !fits_int(L) || !fits_int(D)) return LR_ERR_UNSUPPORTED;
+    const void *ptrs[] = {r, s, x0, y, x_final};
+    for (const void *p : ptrs)
+        if (misaligned(p)) return LR_ERR_MISALIGNED;
+    return LR_OK;
+}
+
 // Decode steps: the state after the step is always written (h_out
 // required); the state before it is optional (NULL = zero).
 int validate_step_common(const void *const *required, int n_required, const void *const *all, int n_all) {
@@ -281,3 +293,23 @@ extern "C" int lr_hgrn2_step(const void *q, const void *k, const void *v, const 
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" size_t lr_minmax_scan_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io) {
+    if (B <= 0 || L <= 0 || D <= 0 || !io_ok(io)) return 0;
+    lr::DiagPlan p;
+    if (lr::minmax_plan(B, L, D, io, &p) != LR_OK) return SIZE_MAX;
+    return p.ws_bytes;
+}
+
+extern "C" int lr_minmax_scan_fwd(const void *r, const void *s, const float *x0, void *y, float *x_final,
+                                  int64_t B, int64_t L, int64_t D, lr_dtype io, void *workspace,
+                                  size_t ws_bytes, lr_stream_t stream) {
+    int rc = validate_minmax(r, s, x0, y, x_final, B, L, D, io);
+    if (rc != LR_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return LR_OK;
+    if (L == 0) return copy_state(x0, x_final, size_t(B) * D, st);
+    lr::DiagPlan p;
+    if ((rc = lr::minmax_plan(B, L, D, io, &p)) != LR_OK) return rc;
+    if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
+    return lr::minmax_launch(r, s, x0, y, x_final, B, L, D, io, p, workspace, st);
+}

@@ -351,6 +351,205 @@ __global__ void __launch_bounds__(RgCfg<IO>::THREADS, 1)  // registers for a who
 }
 
 // ============================================================================
+// MinMax recurrence
+// ============================================================================
+// x_t = max(min(r_t, x_{t-1}), s_t)  (minmaxrnc MinMaxNeuron; the operator
+// f(x) = max(min(a, x), b) of minmax_operator.apply with a = r_t, b = s_t).
+// Same skeleton as the RG-LRU scan: one channel per thread, TMA-staged tiles
+// of r and s, and for time splits a decoupled look-back whose aggregate is
+// the split's composed operator (A, Bc) with f(x) = max(min(A, x), Bc):
+// composing f_t after F gives (min(r_t, A), max(min(r_t, Bc), s_t))
+// (minmax_operator.compose).  min / max select one argument exactly, so the
+// scan is exact in any order; NaN arguments give NaN, as torch.minimum and
+// torch.maximum do.
+__device__ __forceinline__ float min_nan(float a, float b) {
+    float d;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+template <typename IO>
+struct MmCfg {
+    static constexpr int DC = 64;                        // channels per block
+    static constexpr int T = 32;                         // time steps per tile
+    static constexpr int CWARPS = DC / 32;
+    static constexpr int THREADS = 32 * (CWARPS + 1);    // + producer warp
+    static constexpr int STAGES = sizeof(IO) == 2 ? 8 : 5;
+    static constexpr int TILE = T * DC;
+    static constexpr uint32_t STAGE_BYTES = 2u * TILE * sizeof(IO);
+    static constexpr size_t OFF_BAR = size_t(STAGES) * STAGE_BYTES;   // full[], empty[]
+    static constexpr size_t SMEM = OFF_BAR + 2 * STAGES * 8 + 16;
+    static constexpr int kAgg = 2, kIncl = 1;  // (A, Bc) and the inclusive state
+};
+
+template <typename IO, int MODE>
+__device__ __forceinline__ void minmax_tile(const IO *rs, const IO *ss, float &x, float &A, float &Bc,
+                                            IO *yp, int D, int rows) {
+    using C = MmCfg<IO>;
+#pragma unroll
+    for (int j = 0; j < C::T; ++j) {
+        const float r = Io<IO>::to_f(rs[j * C::DC]);
+        const float sv = Io<IO>::to_f(ss[j * C::DC]);
+        if (MODE == kAggregate) {
+            Bc = max_nan(min_nan(r, Bc), sv);
+            A = min_nan(r, A);
+        } else {
+            x = max_nan(min_nan(r, x), sv);
+            if (MODE == kFull) __stcs(yp + size_t(j) * D, Io<IO>::from_f(x));
+            if (MODE == kRagged && j < rows) __stcs(yp + size_t(j) * D, Io<IO>::from_f(x));
+        }
+    }
+}
+
+template <typename IO>
+__global__ void __launch_bounds__(MmCfg<IO>::THREADS, 1)
+    minmax_scan_kernel(const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_s,
+                       const float *__restrict__ x0, IO *__restrict__ y, float *__restrict__ x_final,
+                       int L, int D, int n_db, int S, int tps, int n_tiles, LookbackWs ws,
+                       int withheld, uint64_t timeout_ns) {
+    using C = MmCfg<IO>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    IO *tiles = reinterpret_cast<IO *>(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *empty = full + C::STAGES;
+    int *bcast = reinterpret_cast<int *>(empty + C::STAGES);
+    int *abort_word = bcast + 1;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const BlockAbort ab{abort_word};
+
+    if (tid == 0) {
+        for (int st = 0; st < C::STAGES; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], C::CWARPS);
+        }
+        *abort_word = 0;
+        fence_mbar_init();
+        if (S > 1) *bcast = static_cast<int>(atomicAdd(ws.ticket, 1u));
+    }
+    __syncthreads();
+    const int tk = S > 1 ? *bcast : static_cast<int>(blockIdx.x);
+    const int cb = tk / S, s = tk - (tk / S) * S;
+    const int b = cb / n_db;
+    const int d0 = (cb - b * n_db) * C::DC;
+    const int k0 = s * tps;
+    const int ntl = min(k0 + tps, n_tiles) - k0;
+    const int V = S > 1 ? 2 * ntl : ntl;  // virtual tiles: aggregate pass, then output pass
+
+    if (warp == C::CWARPS) {  // ---------------------------------- producer warp
+        if (lane == 0) {
+            prefetch_tensormap(&tm_r);
+            prefetch_tensormap(&tm_s);
+            for (int v = 0; v < V; ++v) {
+                const int st = v % C::STAGES;
+                if (v >= C::STAGES && !ab.wait(&empty[st], ((v / C::STAGES) - 1) & 1, timeout_ns))
+                    break;
+                const int t0 = (k0 + v % ntl) * C::T;
+                IO *base = tiles + size_t(st) * 2 * C::TILE;
+                mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+                tma_load_3d(base, &tm_r, &full[st], d0, t0, b);
+                tma_load_3d(base + C::TILE, &tm_s, &full[st], d0, t0, b);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ compute warps
+    const int ch = tid;
+    const int d = d0 + ch;
+    const bool vd = d < D;
+    const float x0v = (vd && x0 != nullptr) ? x0[size_t(b) * D + d] : 0.0f;
+    float x = x0v;
+    float A = __int_as_float(0x7f800000), Bc = __int_as_float(0xff800000);  // identity: +inf, -inf
+
+    for (int v = 0; v < V; ++v) {
+        const int st = v % C::STAGES;
+        const bool agg_pass = S > 1 && v < ntl;
+        const int t0 = (k0 + v % ntl) * C::T;
+        ab.wait(&full[st], (v / C::STAGES) & 1, timeout_ns);
+        const IO *rs = tiles + size_t(st) * 2 * C::TILE + ch;
+        const IO *ss = rs + C::TILE;
+        IO *yp = y + (size_t(b) * L + t0) * D + d;
+        const bool full_tile = t0 + C::T <= L && d0 + 32 * (warp + 1) <= D;
+        // rows past L (zero-filled by TMA) must not act: clamp them out of the
+        // aggregate by treating them as identity steps
+        const int rows = vd ? min(C::T, L - t0) : 0;
+        if (agg_pass) {
+            if (t0 + C::T <= L) {
+                minmax_tile<IO, kAggregate>(rs, ss, x, A, Bc, yp, D, 0);
+            } else {
+                for (int j = 0; j < L - t0; ++j) {
+                    const float r = Io<IO>::to_f(rs[j * C::DC]), sv = Io<IO>::to_f(ss[j * C::DC]);
+                    Bc = max_nan(min_nan(r, Bc), sv);
+                    A = min_nan(r, A);
+                }
+            }
+        } else if (full_tile) {
+            minmax_tile<IO, kFull>(rs, ss, x, A, Bc, yp, D, C::T);
+        } else {
+            // the state must not run through the zero-filled rows past L either
+            const float keep = x;
+            float xr = x;
+            for (int j = 0; j < min(C::T, L - t0); ++j) {
+                xr = max_nan(min_nan(Io<IO>::to_f(rs[j * C::DC]), xr), Io<IO>::to_f(ss[j * C::DC]));
+                if (j < rows) __stcs(yp + size_t(j) * D, Io<IO>::from_f(xr));
+            }
+            x = L - t0 > 0 ? xr : keep;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+
+        if (agg_pass && v == ntl - 1) {
+            // ---- publish this split's operator, look back, publish inclusive
+            constexpr int NC = 32 * C::CWARPS;
+            const size_t slot = size_t(cb) * S + s;
+            float carry = x0v;
+            if (s > 0) {
+                ws.agg[(slot * C::kAgg + 0) * C::DC + ch] = A;
+                ws.agg[(slot * C::kAgg + 1) * C::DC + ch] = Bc;
+                __threadfence();
+                named_bar_sync(1, NC);
+                if (tid == 0 && s != withheld) st_release_gpu(&ws.flags[slot], kFlagAggregate);
+                // composition G of splits sp+1 .. s-1 (starts as the identity)
+                float gA = __int_as_float(0x7f800000), gB = __int_as_float(0xff800000);
+                carry = 0.0f;
+                for (int sp = s - 1; sp >= 0; --sp) {
+                    const size_t sl = size_t(cb) * S + sp;
+                    if (tid == 0) *bcast = static_cast<int>(poll_flag(&ws.flags[sl], timeout_ns));
+                    named_bar_sync(1, NC);
+                    const int fv = *bcast;
+                    named_bar_sync(1, NC);
+                    if (fv == static_cast<int>(kFlagInclusive)) {
+                        carry = max_nan(min_nan(gA, __ldcg(&ws.incl[sl * C::DC + ch])), gB);
+                        break;
+                    }
+                    if (fv == static_cast<int>(kFlagAggregate)) {
+                        const float fA = __ldcg(&ws.agg[(sl * C::kAgg + 0) * C::DC + ch]);
+                        const float fB = __ldcg(&ws.agg[(sl * C::kAgg + 1) * C::DC + ch]);
+                        gB = max_nan(min_nan(gA, fB), gB);   // G o F
+                        gA = min_nan(gA, fA);
+                        continue;
+                    }
+                    if (tid == 0) report_status(LR_ERR_TIMEOUT);
+                    carry = max_nan(min_nan(gA, 0.0f), gB);
+                    break;
+                }
+            }
+            ws.incl[slot * C::DC + ch] = max_nan(min_nan(A, carry), Bc);
+            __threadfence();
+            named_bar_sync(1, NC);
+            if (tid == 0 && s != withheld) st_release_gpu(&ws.flags[slot], kFlagInclusive);
+            x = carry;  // the output pass restarts the range from its carry-in
+        }
+    }
+    if (x_final != nullptr && vd && s == S - 1) x_final[size_t(b) * D + d] = x;
+}
+
+// ============================================================================
 // Selective SSM
 // ============================================================================
 // Warp roles in a block of DC channels:
@@ -913,6 +1112,56 @@ int rglru_launch(const void *x, const void *r, const void *i, const float *a_log
                                                     workspace, stream);
     return rglru_launch_t<float, true>(x, r, i, a_log, c, h0, y, h_final, B, L, D, p, workspace,
                                        stream);
+}
+
+// ---------------------------------------------------------------- minmax host
+template <typename IO>
+static int minmax_resident(int dev) {
+    using C = MmCfg<IO>;
+    return kernel_blocks_per_sm<minmax_scan_kernel<IO>>(C::THREADS, C::SMEM, dev);
+}
+
+int minmax_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p) {
+    int sms = 0, dev = 0;
+    if (device_sm_count(&sms) != LR_OK || current_device(&dev) != LR_OK) return LR_ERR_CUDA;
+    *p = DiagPlan{};
+    p->dc = MmCfg<float>::DC;
+    p->tile_t = MmCfg<float>::T;
+    p->n_cb = B * ((D + p->dc - 1) / p->dc);
+    p->n_tiles = static_cast<int>((L + p->tile_t - 1) / p->tile_t);
+    const int per_sm = io == LR_BF16 ? minmax_resident<__nv_bfloat16>(dev) : minmax_resident<float>(dev);
+    if (per_sm <= 0) return LR_ERR_CUDA;
+    choose_splits(p, sms, per_sm, MmCfg<float>::kAgg, MmCfg<float>::kIncl);
+    return LR_OK;
+}
+
+template <typename IO>
+static int minmax_launch_t(const void *r, const void *s, const float *x0, void *y, float *x_final,
+                           int64_t B, int64_t L, int64_t D, const DiagPlan &p, void *workspace,
+                           cudaStream_t stream) {
+    using C = MmCfg<IO>;
+    CUtensorMap mr, ms;
+    const auto tt = Io<IO>::kTmType;
+    if (!make_map_3d(&mr, r, tt, sizeof(IO), D, L, B, C::DC, C::T) ||
+        !make_map_3d(&ms, s, tt, sizeof(IO), D, L, B, C::DC, C::T))
+        return LR_ERR_CUDA;
+    if (p.S > 1 && cudaMemsetAsync(workspace, 0, p.ctrl_bytes, stream) != cudaSuccess)
+        return LR_ERR_CUDA;
+    const LookbackWs ws = carve(p, workspace, C::kAgg);
+    const int n_db = static_cast<int>((D + C::DC - 1) / C::DC);
+    const int64_t grid = p.n_cb * p.S;
+    minmax_scan_kernel<IO><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(
+        mr, ms, x0, static_cast<IO *>(y), x_final, static_cast<int>(L), static_cast<int>(D), n_db, p.S,
+        p.tps, p.n_tiles, ws, g_withheld_split, timeout_ns());
+    return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+int minmax_launch(const void *r, const void *s, const float *x0, void *y, float *x_final, int64_t B,
+                  int64_t L, int64_t D, lr_dtype io, const DiagPlan &p, void *workspace,
+                  cudaStream_t stream) {
+    if (io == LR_BF16)
+        return minmax_launch_t<__nv_bfloat16>(r, s, x0, y, x_final, B, L, D, p, workspace, stream);
+    return minmax_launch_t<float>(r, s, x0, y, x_final, B, L, D, p, workspace, stream);
 }
 
 // ------------------------------------------------------------- selective host

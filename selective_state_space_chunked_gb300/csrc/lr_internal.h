@@ -46,6 +46,11 @@ int selective_launch(const void *x, const void *dt, const void *z, const void *B
                      void *y, float *h_final, int64_t B, int64_t L, int64_t D, lr_dtype io,
                      int dt_softplus, const DiagPlan &p, void *workspace, cudaStream_t stream);
 
+int minmax_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p);
+int minmax_launch(const void *r, const void *s, const float *x0, void *y, float *x_final, int64_t B,
+                  int64_t L, int64_t D, lr_dtype io, const DiagPlan &p, void *workspace,
+                  cudaStream_t stream);
+
 int diag_status_read_and_clear(int *status);
 
 // Built-in scratch of lr_rglru_scan_fwd_noalloc (1 MiB per device).

@@ -207,3 +207,19 @@ def test_steps_with_no_elements_launch_nothing(lr):
     assert call_sel_step(lr, B=0, x=None, y=None, h_out=None) == 0
     assert call_rg_step(lr, D=0, x=None, y=None, h_out=None) == 0
     assert call_hg_step(lr, B=0, q=None, o=None, S_out=None) == 0
+
+
+def call_mm(lr, **kw):
+    a = dict(r=FAKE, s=FAKE, x0=FAKE, y=FAKE, x_final=FAKE, B=2, L=64, D=64, io=1,
+             workspace=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lr.lr_minmax_scan_fwd(*a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(r=None), -1), (dict(s=None), -1), (dict(y=None), -1), (dict(B=-1), -1),
+    (dict(io=4), -1), (dict(D=12), -2), (dict(D=6, io=0), -2), (dict(L=1 << 40), -2),
+    (dict(x0=FAKE + 4), -3), (dict(x_final=FAKE + 8), -3),
+])
+def test_minmax_validation_codes(lr, kw, code):
+    assert call_mm(lr, **kw) == code
