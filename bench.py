@@ -331,29 +331,48 @@ def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
     """Scans outside the step, timed the same way (inputs larger than L2,
     CUDA events on the launching stream): the MinMax recurrence at the
     RG-LRU workload's shape, bf16 I/O."""
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    def entry(name, ms, units, by):
+        gbs = by / (ms * 1e-3) / 1e9
+        return {"workload": name, "ms": ms, "tok_ch_per_s": units / (ms * 1e-3), "gb_per_s": gbs,
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}}
+
+    res = []
     B, L, D = 8, 4096, 2560
     g = torch.Generator(device=dev).manual_seed(11)
     r = torch.randn(B, L, D, device=dev, generator=g).to(torch.bfloat16)
     s_ = (torch.randn(B, L, D, device=dev, generator=g) - 1.0).to(torch.bfloat16)
     x0 = torch.randn(B, D, device=dev, generator=g)
-    fn = lambda: lr.minmax_scan(r, s_, x0)
-    for _ in range(3):
-        fn()
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(reps)]
-    for a, b in ev:
-        a.record()
-        fn()
-        b.record()
-    torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
-    by = 3 * 2 * B * L * D + 2 * 4 * B * D
-    gbs = by / (ms * 1e-3) / 1e9
-    return [{"workload": f"minmax_bf16_B{B}_L{L}_D{D}", "ms": ms,
-             "tok_ch_per_s": B * L * D / (ms * 1e-3), "gb_per_s": gbs,
-             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}}]
+    res.append(entry(f"minmax_bf16_B{B}_L{L}_D{D}", timed(lambda: lr.minmax_scan(r, s_, x0)),
+                     B * L * D, 3 * 2 * B * L * D + 2 * 4 * B * D))
+    del r, s_
+    # the RG-LRU and HGRN2 workloads with their gates before the activation
+    # (sigmoid / lower-bounded sigmoid applied in the kernel)
+    cfg = wl.CONFIGS[2]
+    p = wl.make_inputs(cfg, device=dev)
+    res.append(entry(cfg.name + " gates_preact", timed(lambda: lr.rglru_scan(
+        p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"], gates_preact=True)),
+        cfg.B * cfg.L * cfg.D, algorithmic(cfg)["bytes"]))
+    del p
+    cfg = wl.CONFIGS[4]
+    p = wl.make_inputs(cfg, device=dev)
+    res.append(entry(cfg.name + " gate_lb=0.2", timed(lambda: lr.hgrn2(
+        p["q"], p["k"], p["v"], p["g"], H=p["H"], gate_lb=0.2)),
+        algorithmic(cfg)["units"], algorithmic(cfg)["bytes"]))
+    return res
 
 
 def input_bytes(p) -> int:

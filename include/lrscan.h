@@ -212,6 +212,32 @@ int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g,
                  void *workspace, size_t ws_bytes, lr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Gates given before their activation                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The pages activate the gates right before their scans: [RGLRU] forward
+ * applies sigmoid to the r and i projections, [HGRN2] lower-bounds a
+ * sigmoid-activated forget gate, g = lb + (1 - lb) sigmoid(f).  These entry
+ * points take the pre-activation tensors and apply the activation inside the
+ * scan kernel, so callers need no separate elementwise pass; otherwise they
+ * are lr_rglru_scan_fwd and lr_hgrn2_fwd (same layouts, requirements,
+ * workspace and errors).  lr_hgrn2_preact_fwd: lb in [0, 1) (else
+ * LR_ERR_INVALID_ARG); f is (B, L, H*dv) like g.
+ */
+int lr_rglru_scan_preact_fwd(const void *x, const void *r_pre, const void *i_pre,
+                             const float *a_log, float c, const float *h0,
+                             void *y, float *h_final,
+                             int64_t B, int64_t L, int64_t D, lr_dtype io,
+                             void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+int lr_hgrn2_preact_fwd(const void *q, const void *k, const void *v, const void *f,
+                        float lb, const float *S0, void *o, float *S_final,
+                        int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
+                        int64_t chunk, lr_dtype io,
+                        void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* MinMax recurrence                                                         */
 /* ------------------------------------------------------------------------ */
 

@@ -49,6 +49,10 @@ SIGNATURES = {
     "lr_hgrn2_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I]),
     "lr_hgrn2_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                           _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_rglru_scan_preact_fwd": (_I, [_P, _P, _P, _P, _F, _P, _P, _P,
+                                      _I64, _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_hgrn2_preact_fwd": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                 _I64, _I64, _I, _P, _SZ, _P]),
     "lr_minmax_scan_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
     "lr_minmax_scan_fwd": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, _SZ, _P]),
     "lr_selective_scan_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -143,6 +147,18 @@ def lr_hgrn2_fwd(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io,
                  workspace, ws_bytes, stream) -> int:
     return int(_lib.lr_hgrn2_fwd(q, k, v, g, S0, o, S_final, B, L, H, dk, dv,
                                  chunk, io, workspace, ws_bytes, stream))
+
+
+def lr_rglru_scan_preact_fwd(x, r_pre, i_pre, a_log, c, h0, y, h_final, B, L, D, io,
+                             workspace, ws_bytes, stream) -> int:
+    return int(_lib.lr_rglru_scan_preact_fwd(x, r_pre, i_pre, a_log, c, h0, y, h_final, B, L, D,
+                                             io, workspace, ws_bytes, stream))
+
+
+def lr_hgrn2_preact_fwd(q, k, v, f, lb, S0, o, S_final, B, L, H, dk, dv, chunk, io,
+                        workspace, ws_bytes, stream) -> int:
+    return int(_lib.lr_hgrn2_preact_fwd(q, k, v, f, lb, S0, o, S_final, B, L, H, dk, dv, chunk,
+                                        io, workspace, ws_bytes, stream))
 
 
 def lr_minmax_scan_workspace_size(B, L, D, io) -> int:
@@ -289,8 +305,9 @@ def selective_scan(x, dt, Bm, Cm, A_log, z=None, Dskip=None, h0=None,
 
 
 def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None, out=None,
-               sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
-    """RG-LRU scan.  x, r, i: (B, L, D) (r, i after their sigmoid), one dtype;
+               sync_host: bool = True, gates_preact: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """RG-LRU scan.  x, r, i: (B, L, D) (r, i after their sigmoid, or before
+    it with ``gates_preact=True``: the kernel applies it), one dtype;
     a_log: (D,) fp32; h0: (B, D) fp32.  Returns (y (B, L, D), h_final (B, D)
     fp32); ``out=(y, h_final)`` gives the result tensors (GPU or host)."""
     host = x.device.type != "cuda"
@@ -303,19 +320,21 @@ def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None, out=None
     (y, hf), host_out = _outputs(out, [((B, L, D), x.dtype), ((B, D), torch.float32)], dev)
     ws, wsb = _workspace(lr_rglru_scan_workspace_size(B, L, D, io), dev, workspace)
     stream = torch.cuda.current_stream(dev).cuda_stream
-    _check(lr_rglru_scan_fwd(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c),
-                             _ptr(h0), _ptr(y), _ptr(hf), B, L, D, io, _ptr(ws),
-                             wsb, stream), "lr_rglru_scan_fwd")
+    fwd = lr_rglru_scan_preact_fwd if gates_preact else lr_rglru_scan_fwd
+    _check(fwd(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c), _ptr(h0), _ptr(y), _ptr(hf),
+               B, L, D, io, _ptr(ws), wsb, stream), fwd.__name__)
     return _finish((y, hf), host_out, host, dev, sync_host)
 
 
 def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None,
-          sync_host: bool = True) -> Tuple[torch.Tensor, torch.Tensor]:
+          sync_host: bool = True, gate_lb: Optional[float] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """HGRN2 matrix-state recurrence.  q, k: (B, L, H*dk); v, g: (B, L, H*dv)
-    (g after its activation and lower bound), bfloat16; S0: (B, H, dv, dk)
-    fp32.  Returns (o (B, L, H*dv), S_final (B, H, dv, dk) fp32);
-    ``out=(o, S_final)`` gives the result tensors (GPU or host).  Raises
-    ValueError when the hidden size is not divisible by the head count."""
+    (g after its activation and lower bound; with ``gate_lb`` set, g is the
+    pre-activation f and the kernel forms lb + (1 - lb) sigmoid(f)),
+    bfloat16; S0: (B, H, dv, dk) fp32.  Returns (o (B, L, H*dv), S_final
+    (B, H, dv, dk) fp32); ``out=(o, S_final)`` gives the result tensors (GPU
+    or host).  Raises ValueError when the hidden size is not divisible by
+    the head count."""
     if q.shape[-1] % H or v.shape[-1] % H:
         raise ValueError(f"hidden size {q.shape[-1]} is not divisible by {H} heads")
     host = q.device.type != "cuda"
@@ -330,9 +349,14 @@ def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None
                                  dev)
     ws, wsb = _workspace(lr_hgrn2_workspace_size(B, L, H, dk, dv, io), dev, workspace)
     stream = torch.cuda.current_stream(dev).cuda_stream
-    _check(lr_hgrn2_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0), _ptr(o),
-                        _ptr(Sf), B, L, H, dk, dv, chunk, io, _ptr(ws), wsb,
-                        stream), "lr_hgrn2_fwd")
+    if gate_lb is None:
+        _check(lr_hgrn2_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0), _ptr(o),
+                            _ptr(Sf), B, L, H, dk, dv, chunk, io, _ptr(ws), wsb,
+                            stream), "lr_hgrn2_fwd")
+    else:
+        _check(lr_hgrn2_preact_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(gate_lb), _ptr(S0),
+                                   _ptr(o), _ptr(Sf), B, L, H, dk, dv, chunk, io, _ptr(ws), wsb,
+                                   stream), "lr_hgrn2_preact_fwd")
     return _finish((o, Sf), host_out, host, dev, sync_host)
 
 

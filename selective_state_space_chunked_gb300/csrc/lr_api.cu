@@ -313,3 +313,41 @@ extern "C" int lr_minmax_scan_fwd(const void *r, const void *s, const float *x0,
     if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
     return lr::minmax_launch(r, s, x0, y, x_final, B, L, D, io, p, workspace, st);
 }
+
+// RG-LRU with the gates given before their sigmoid ([RGLRU] forward applies
+// sigmoid to the r and i projections before the scan); the sigmoid runs in
+// the scan kernel.  Same workspace as lr_rglru_scan_fwd.
+extern "C" int lr_rglru_scan_preact_fwd(const void *x, const void *r_pre, const void *i_pre,
+                                        const float *a_log, float c, const float *h0, void *y,
+                                        float *h_final, int64_t B, int64_t L, int64_t D, lr_dtype io,
+                                        void *workspace, size_t ws_bytes, lr_stream_t stream) {
+    int rc = validate_rglru(x, r_pre, i_pre, a_log, c, h0, y, h_final, B, L, D, io);
+    if (rc != LR_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (B == 0 || D == 0) return LR_OK;
+    if (L == 0) return copy_state(h0, h_final, size_t(B) * D, st);
+    lr::DiagPlan p;
+    if ((rc = lr::rglru_plan(B, L, D, io, &p)) != LR_OK) return rc;
+    if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
+    return lr::rglru_launch(x, r_pre, i_pre, a_log, c, h0, y, h_final, B, L, D, io, p, workspace, st,
+                            true);
+}
+
+// HGRN2 with the forget gate given as its pre-activation f: the kernel forms
+// g = lb + (1 - lb) sigmoid(f) ([HGRN2] sigmoid-activated, lower-bounded
+// gate) before the recurrence.  lb in [0, 1).
+extern "C" int lr_hgrn2_preact_fwd(const void *q, const void *k, const void *v, const void *f, float lb,
+                                   const float *S0, void *o, float *S_final, int64_t B, int64_t L,
+                                   int64_t H, int64_t dk, int64_t dv, int64_t chunk, lr_dtype io,
+                                   void *workspace, size_t ws_bytes, lr_stream_t stream) {
+    if (!(lb >= 0.0f && lb < 1.0f)) return LR_ERR_INVALID_ARG;
+    int rc = validate_hgrn2(q, k, v, f, S0, o, S_final, B, L, H, dk, dv, chunk, io);
+    if (rc != LR_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (B == 0) return LR_OK;
+    if (L == 0) return copy_state(S0, S_final, size_t(B) * H * dv * dk, st);
+    size_t need = 0;
+    if ((rc = lr::hgrn2_workspace(B, L, H, &need)) != LR_OK) return rc;
+    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return LR_ERR_WORKSPACE;
+    return lr::hgrn2_launch(q, k, v, f, S0, o, S_final, B, L, H, workspace, st, true, lb);
+}

@@ -196,8 +196,16 @@ __device__ __forceinline__ void rglru_ab(float r, float u, float cl, float cl2, 
 // scheduler can interleave), and a ragged output tile.
 enum TileMode { kAggregate = 0, kFull = 1, kRagged = 2 };
 
-// One T-step tile of one channel's recurrence.
-template <typename IO, bool ACC, int MODE>
+// Logistic sigmoid of a pre-activation gate.
+template <bool ACC>
+__device__ __forceinline__ float sigmoid_t(float v) {
+    return ACC ? 1.0f / (1.0f + expf(-v)) : rcp_approx(1.0f + ex2_approx(-v * kLog2e));
+}
+
+// One T-step tile of one channel's recurrence.  PRE: r and i arrive before
+// their sigmoid, which is applied here.  `rows` = steps of the tile inside
+// the sequence (0 for a channel past D).
+template <typename IO, bool ACC, bool PRE, int MODE>
 __device__ __forceinline__ void rglru_tile(const IO *xs, const IO *rs, const IO *is, float cl,
                                            float cl2, float &h, float &P, IO *yp, int D, int rows) {
     using C = RgCfg<IO>;
@@ -207,8 +215,18 @@ __device__ __forceinline__ void rglru_tile(const IO *xs, const IO *rs, const IO 
 #pragma unroll
         for (int u = 0; u < C::BATCH; ++u) {
             const int o = (j0 + u) * C::DC;
-            rglru_ab<ACC>(Io<IO>::to_f(rs[o]), Io<IO>::to_f(is[o]) * Io<IO>::to_f(xs[o]), cl, cl2,
-                          a[u], bb[u]);
+            float rv = Io<IO>::to_f(rs[o]), iv = Io<IO>::to_f(is[o]);
+            if (PRE) {
+                rv = sigmoid_t<ACC>(rv);
+                iv = sigmoid_t<ACC>(iv);
+            }
+            rglru_ab<ACC>(rv, iv * Io<IO>::to_f(xs[o]), cl, cl2, a[u], bb[u]);
+            // rows past L arrive zero-filled; with raw gates r = 0 is the
+            // identity step (a = 1, b = 0), after a sigmoid it is not
+            if (PRE && MODE != kFull && j0 + u >= rows) {
+                a[u] = 1.0f;
+                bb[u] = 0.0f;
+            }
         }
 #pragma unroll
         for (int u = 0; u < C::BATCH; ++u) {
@@ -220,7 +238,7 @@ __device__ __forceinline__ void rglru_tile(const IO *xs, const IO *rs, const IO 
     }
 }
 
-template <typename IO, bool ACC>
+template <typename IO, bool ACC, bool PRE>
 __global__ void __launch_bounds__(RgCfg<IO>::THREADS, 1)  // registers for a whole batch in flight
     rglru_scan_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_r,
                       const __grid_constant__ CUtensorMap tm_i, const float *__restrict__ a_log,
@@ -297,11 +315,12 @@ __global__ void __launch_bounds__(RgCfg<IO>::THREADS, 1)  // registers for a who
         // warp-uniform choice: the whole warp's channels and rows in range?
         const bool full_tile = t0 + C::T <= L && d0 + 32 * (warp + 1) <= D;
         if (agg_pass)
-            rglru_tile<IO, ACC, kAggregate>(xs, rs, is, cl, cl2, h, P, yp, D, 0);
+            rglru_tile<IO, ACC, PRE, kAggregate>(xs, rs, is, cl, cl2, h, P, yp, D, min(C::T, L - t0));
         else if (full_tile)
-            rglru_tile<IO, ACC, kFull>(xs, rs, is, cl, cl2, h, P, yp, D, C::T);
+            rglru_tile<IO, ACC, PRE, kFull>(xs, rs, is, cl, cl2, h, P, yp, D, C::T);
         else
-            rglru_tile<IO, ACC, kRagged>(xs, rs, is, cl, cl2, h, P, yp, D, vd ? min(C::T, L - t0) : 0);
+            rglru_tile<IO, ACC, PRE, kRagged>(xs, rs, is, cl, cl2, h, P, yp, D,
+                                              vd ? min(C::T, L - t0) : 0);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
 
@@ -1064,7 +1083,13 @@ int device_sm_count(int *sms) {
 // ---------------------------------------------------------------- RG-LRU host
 template <typename IO, bool ACC>
 static int rglru_resident(int dev) {
-    return kernel_blocks_per_sm<rglru_scan_kernel<IO, ACC>>(RgCfg<IO>::THREADS, RgCfg<IO>::SMEM, dev);
+    // both gate variants share block size and shared memory; each needs its
+    // own dynamic shared-memory attribute
+    const int a = kernel_blocks_per_sm<rglru_scan_kernel<IO, ACC, false>>(RgCfg<IO>::THREADS,
+                                                                          RgCfg<IO>::SMEM, dev);
+    const int b = kernel_blocks_per_sm<rglru_scan_kernel<IO, ACC, true>>(RgCfg<IO>::THREADS,
+                                                                         RgCfg<IO>::SMEM, dev);
+    return a < b ? a : b;
 }
 
 int rglru_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p) {
@@ -1085,7 +1110,8 @@ int rglru_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p) {
 template <typename IO, bool ACC>
 static int rglru_launch_t(const void *x, const void *r, const void *i, const float *a_log, float c,
                           const float *h0, void *y, float *h_final, int64_t B, int64_t L,
-                          int64_t D, const DiagPlan &p, void *workspace, cudaStream_t stream) {
+                          int64_t D, const DiagPlan &p, void *workspace, bool preact,
+                          cudaStream_t stream) {
     using C = RgCfg<IO>;
     CUtensorMap mx, mr, mi;
     const auto tt = Io<IO>::kTmType;
@@ -1098,7 +1124,8 @@ static int rglru_launch_t(const void *x, const void *r, const void *i, const flo
     const LookbackWs ws = carve(p, workspace, C::kAgg);
     const int n_db = static_cast<int>((D + C::DC - 1) / C::DC);
     const int64_t grid = p.n_cb * p.S;
-    rglru_scan_kernel<IO, ACC><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(
+    auto kern = preact ? rglru_scan_kernel<IO, ACC, true> : rglru_scan_kernel<IO, ACC, false>;
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, stream>>>(
         mx, mr, mi, a_log, c, h0, static_cast<IO *>(y), h_final, static_cast<int>(L),
         static_cast<int>(D), n_db, p.S, p.tps, p.n_tiles, ws, g_withheld_split, timeout_ns());
     return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
@@ -1106,12 +1133,12 @@ static int rglru_launch_t(const void *x, const void *r, const void *i, const flo
 
 int rglru_launch(const void *x, const void *r, const void *i, const float *a_log, float c,
                  const float *h0, void *y, float *h_final, int64_t B, int64_t L, int64_t D,
-                 lr_dtype io, const DiagPlan &p, void *workspace, cudaStream_t stream) {
+                 lr_dtype io, const DiagPlan &p, void *workspace, cudaStream_t stream, bool preact) {
     if (io == LR_BF16)
         return rglru_launch_t<__nv_bfloat16, false>(x, r, i, a_log, c, h0, y, h_final, B, L, D, p,
-                                                    workspace, stream);
+                                                    workspace, preact, stream);
     return rglru_launch_t<float, true>(x, r, i, a_log, c, h0, y, h_final, B, L, D, p, workspace,
-                                       stream);
+                                       preact, stream);
 }
 
 // ---------------------------------------------------------------- minmax host

@@ -135,11 +135,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 }  // namespace hg
 
+// PRE: the gate arrives as the pre-activation f and the front forms
+// g = lb + (1 - lb) sigmoid(f) ([HGRN2] lower-bounded, sigmoid-activated gate).
+template <bool PRE>
 __global__ void __launch_bounds__(hg::THREADS, 1)
     hgrn2_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                        const float *__restrict__ S0, float *__restrict__ S_final,
-                       __nv_bfloat16 *__restrict__ o, int L, int H, int n_chunks,
+                       __nv_bfloat16 *__restrict__ o, int L, int H, int n_chunks, float lb,
                        uint64_t timeout_ns) {
     using namespace hg;
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -322,7 +325,8 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
 #pragma unroll
             for (int u = 0; u < FSTEPS; ++u) {
                 const int t = tb + u;
-                const float gv = __bfloat162float(sG[t * RB + i]);
+                float gv = __bfloat162float(sG[t * RB + i]);
+                if (PRE) gv = fmaf(1.0f - lb, rcp_approx(1.0f + ex2_approx(-gv * kLog2e)), lb);
                 acc += t0 + t < L ? lg2_approx(gv) : 0.0f;
                 loc[u] = acc;
             }
@@ -545,7 +549,9 @@ bool hg_setup_once() {
     static std::once_flag once;
     static bool ok = false;
     std::call_once(once, [] {
-        ok = cudaFuncSetAttribute(hgrn2_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        ok = cudaFuncSetAttribute(hgrn2_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(hg::SMEM)) == cudaSuccess &&
+             cudaFuncSetAttribute(hgrn2_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(hg::SMEM)) == cudaSuccess;
     });
     return ok;
@@ -560,7 +566,7 @@ int hgrn2_workspace(int64_t, int64_t, int64_t, size_t *bytes) {
 
 int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                  void *o, float *S_final, int64_t B, int64_t L, int64_t H, void *,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, bool preact, float lb) {
     const uint64_t HK = uint64_t(H) * hg::DK, HV = uint64_t(H) * hg::DV;
     CUtensorMap mq, mk, mv, mg;
     if (!hg_map(&mq, q, HK, L, B, 64, true) || !hg_map(&mk, k, HK, L, B, 64, true) ||
@@ -571,9 +577,10 @@ int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, con
     const int64_t grid = B * H * hg::NRB;
     const uint64_t timeout = g_withheld_split >= 1 ? uint64_t(g_withheld_timeout_ms) * 1000000ull
                                                    : kDefaultTimeoutNs;
-    hgrn2_chunk_kernel<<<static_cast<unsigned>(grid), hg::THREADS, hg::SMEM, stream>>>(
+    auto kern = preact ? hgrn2_chunk_kernel<true> : hgrn2_chunk_kernel<false>;
+    kern<<<static_cast<unsigned>(grid), hg::THREADS, hg::SMEM, stream>>>(
         mq, mk, mv, mg, S0, S_final, static_cast<__nv_bfloat16 *>(o), static_cast<int>(L),
-        static_cast<int>(H), n_chunks, timeout);
+        static_cast<int>(H), n_chunks, lb, timeout);
     return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 

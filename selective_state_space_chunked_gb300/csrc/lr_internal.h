@@ -38,7 +38,8 @@ int device_sm_count(int *sms);  // LR_OK / LR_ERR_CUDA
 int rglru_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p);
 int rglru_launch(const void *x, const void *r, const void *i, const float *a_log, float c,
                  const float *h0, void *y, float *h_final, int64_t B, int64_t L, int64_t D,
-                 lr_dtype io, const DiagPlan &p, void *workspace, cudaStream_t stream);
+                 lr_dtype io, const DiagPlan &p, void *workspace, cudaStream_t stream,
+                 bool preact = false);
 
 int selective_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p);
 int selective_launch(const void *x, const void *dt, const void *z, const void *Bm,
@@ -61,7 +62,7 @@ int rglru_builtin_scratch(void **ptr);  // device address, set up once per devic
 int hgrn2_workspace(int64_t B, int64_t L, int64_t H, size_t *bytes);
 int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                  void *o, float *S_final, int64_t B, int64_t L, int64_t H, void *workspace,
-                 cudaStream_t stream);
+                 cudaStream_t stream, bool preact = false, float lb = 0.0f);
 int hgrn2_status_read_and_clear(int *status);
 
 // Single-token decode steps (plain one-pass kernels)

@@ -223,3 +223,19 @@ def call_mm(lr, **kw):
 ])
 def test_minmax_validation_codes(lr, kw, code):
     assert call_mm(lr, **kw) == code
+
+
+@pytest.mark.parametrize("lb", [1.0, -0.1, float("nan")])
+def test_hgrn2_preact_rejects_lower_bound_outside_unit_interval(lr, lb):
+    a = hg_args()
+    a = dict(q=a["q"], k=a["k"], v=a["v"], f=a["g"], lb=lb, S0=a["S0"], o=a["o"],
+             S_final=a["S_final"], B=2, L=64, H=4, dk=128, dv=128, chunk=64, io=1,
+             workspace=None, ws_bytes=0, stream=None)
+    assert lr.lr_hgrn2_preact_fwd(*a.values()) == lr.LR_ERR_INVALID_ARG
+
+
+def test_rglru_preact_validation_matches_plain(lr):
+    a = rg_args(r=None)
+    assert lr.lr_rglru_scan_preact_fwd(*a.values()) == lr.LR_ERR_INVALID_ARG
+    a = rg_args(D=12)
+    assert lr.lr_rglru_scan_preact_fwd(*a.values()) == lr.LR_ERR_UNSUPPORTED
