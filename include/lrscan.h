@@ -195,9 +195,14 @@ int lr_rglru_scan_fwd_noalloc(const void *x, const void *r, const void *i,
  *
  * Layouts: q, k: (B, L, H*dk); v, g, o: (B, L, H*dv), all in `io`;
  *          S0, S_final: (B, H, dv, dk) fp32.  Optional: S0, S_final.
- * Requirements: H > 0; dk == dv == 128; chunk == 64; io == LR_BF16; else
- *          LR_ERR_UNSUPPORTED.  Within every chunk of 64 steps the product
- *          of a channel's gates must stay above 2^-160 (always true when
+ * Requirements: H > 0, dk >= 1, dv >= 1, chunk >= 1; dk <= 512 (else
+ *          LR_ERR_UNSUPPORTED).
+ * Two kernels: dk == dv == 128 with chunk == 64 and bf16 I/O runs the
+ *          chunked tcgen05 tensor-core kernel; every other shape or fp32 I/O
+ *          runs a step-by-step CUDA-core kernel (fp32 arithmetic throughout,
+ *          O(L dk dv) work, no gate-range limit; `chunk` is not used there).
+ *          On the tensor-core path the product of a channel's gates within
+ *          every chunk of 64 steps must stay above 2^-160 (always true when
  *          g >= 0.18, e.g. with a lower bound of 0.2); otherwise the kernel
  *          sets LR_ERR_RANGE and that chunk's outputs are not meaningful.
  * No workspace is needed (lr_hgrn2_workspace_size returns 0).

@@ -82,12 +82,18 @@ int validate_hgrn2(const void *q, const void *k, const void *v, const void *g, c
     if (B < 0 || L < 0 || H <= 0 || dk <= 0 || dv <= 0 || chunk <= 0 || !io_ok(io))
         return LR_ERR_INVALID_ARG;
     if (B > 0 && L > 0 && (!q || !k || !v || !g || !o)) return LR_ERR_INVALID_ARG;
-    if (dk != 128 || dv != 128 || chunk != 64 || io != LR_BF16) return LR_ERR_UNSUPPORTED;
+    if (dk > 512) return LR_ERR_UNSUPPORTED;
     if (!fits_int(B) || !fits_int(L) || !fits_int(H) || !fits_int(B * H)) return LR_ERR_UNSUPPORTED;
     const void *ptrs[] = {q, k, v, g, S0, o, S_final};
     for (const void *p : ptrs)
         if (misaligned(p)) return LR_ERR_MISALIGNED;
     return LR_OK;
+}
+
+// The tcgen05 chunked kernel serves dk = dv = 128, chunk 64, bf16 I/O; every
+// other case runs on the general step-by-step kernel.
+bool hgrn2_tensor_path(int64_t dk, int64_t dv, int64_t chunk, lr_dtype io) {
+    return dk == 128 && dv == 128 && chunk == 64 && io == LR_BF16;
 }
 
 int validate_minmax(const void *r, const void *s, const float *x0, const void *y, const float *x_final,
@@ -244,6 +250,9 @@ int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g, con
     if ((rc = lr::hgrn2_workspace(B, L, H, &need)) != LR_OK) return rc;
     if (need > 0 && (workspace == nullptr || ws_bytes < need)) return LR_ERR_WORKSPACE;
     if (misaligned(workspace)) return LR_ERR_MISALIGNED;
+    if (!hgrn2_tensor_path(dk, dv, chunk, io))
+        return lr::hgrn2_general_launch(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, io == LR_BF16,
+                                        false, 0.0f, st);
     return lr::hgrn2_launch(q, k, v, g, S0, o, S_final, B, L, H, workspace, st);
 }
 
@@ -349,5 +358,8 @@ extern "C" int lr_hgrn2_preact_fwd(const void *q, const void *k, const void *v, 
     size_t need = 0;
     if ((rc = lr::hgrn2_workspace(B, L, H, &need)) != LR_OK) return rc;
     if (need > 0 && (workspace == nullptr || ws_bytes < need)) return LR_ERR_WORKSPACE;
+    if (!hgrn2_tensor_path(dk, dv, chunk, io))
+        return lr::hgrn2_general_launch(q, k, v, f, S0, o, S_final, B, L, H, dk, dv, io == LR_BF16,
+                                        true, lb, st);
     return lr::hgrn2_launch(q, k, v, f, S0, o, S_final, B, L, H, workspace, st, true, lb);
 }

@@ -64,6 +64,10 @@ int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, con
                  void *o, float *S_final, int64_t B, int64_t L, int64_t H, void *workspace,
                  cudaStream_t stream, bool preact = false, float lb = 0.0f);
 int hgrn2_status_read_and_clear(int *status);
+// HGRN2 for fp32 I/O and head dims other than 128 x 128 (CUDA cores, step by step)
+int hgrn2_general_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
+                         void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
+                         int64_t dv, int io_bf16, bool preact, float lb, cudaStream_t stream);
 
 // Single-token decode steps (plain one-pass kernels)
 int selective_step_launch(const void *x, const void *dt, const void *z, const void *Bm, const void *Cm,

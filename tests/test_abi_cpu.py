@@ -121,7 +121,7 @@ def call_hg(lr, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), -1), (dict(g=None), -1), (dict(o=None), -1),
     (dict(H=0), -1), (dict(dk=0), -1), (dict(chunk=0), -1), (dict(B=-2), -1),
-    (dict(dk=64), -2), (dict(dv=96), -2), (dict(chunk=32), -2), (dict(io=0), -2),
+    (dict(dk=513), -2), (dict(dk=4096), -2),
     (dict(k=FAKE + 2), -3), (dict(S0=FAKE + 4), -3),
 ])
 def test_hgrn2_validation_codes(lr, kw, code):

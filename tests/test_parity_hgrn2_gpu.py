@@ -102,3 +102,60 @@ def test_hgrn2_config4_full_size_sampled(lr):
         orf, Srf = oracle.hgrn2(sub["q"], sub["k"], sub["v"], sub["g"], 1)
         assert rel_err(o[b:b + 1, :, sl].float().cpu(), orf) <= TOL
         assert rel_err(Sf[b:b + 1, h:h + 1].cpu(), Srf) <= TOL
+
+
+# ---------------------------------------------------------------- general path
+# fp32 I/O, head dims other than 128 x 128 and chunk lengths other than 64 run
+# the step-by-step CUDA-core kernel; fp32 I/O meets the 1e-4 bar there.
+def general_inputs(B, L, H, dk, dv, seed, dtype):
+    g = torch.Generator().manual_seed(seed)
+    q, k = (torch.randn(B, L, H * dk, generator=g) / dk ** 0.5 for _ in range(2))
+    v = torch.randn(B, L, H * dv, generator=g) / dv ** 0.5
+    gate = 0.2 + 0.8 * torch.sigmoid(torch.randn(B, L, H * dv, generator=g) + 2)
+    return {"q": q.to(dtype), "k": k.to(dtype), "v": v.to(dtype), "g": gate.to(dtype), "H": H}
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.float32, 1e-4), (torch.bfloat16, 1e-2)])
+@pytest.mark.parametrize("B,L,H,dk,dv", [(2, 200, 2, 128, 128), (1, 150, 3, 64, 32),
+                                         (1, 97, 1, 40, 24), (1, 64, 2, 256, 128),
+                                         (1, 33, 1, 300, 16)])
+def test_hgrn2_general_path_matches_oracle(lr, dtype, tol, B, L, H, dk, dv):
+    if dtype == torch.bfloat16 and dk == dv == 128:
+        pytest.skip("bf16 128 x 128 runs the tensor-core kernel (covered above)")
+    p = general_inputs(B, L, H, dk, dv, seed=B + L + dk, dtype=dtype)
+    S0 = 0.1 * torch.randn(B, H, dv, dk, generator=torch.Generator().manual_seed(L))
+    o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), p["g"].cuda(), H=H, S0=S0.cuda())
+    torch.cuda.synchronize()
+    assert lr.lr_check_status(0) == 0
+    orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], H, S0=S0)
+    assert rel_err(o.float().cpu(), orf) <= tol
+    assert rel_err(Sf.cpu(), Srf) <= tol
+
+
+def test_hgrn2_general_path_other_chunk_and_preact(lr):
+    """128 x 128 bf16 with chunk != 64 takes the general kernel; with the gate
+    given before its activation as well."""
+    p = wl.hgrn2_inputs(1, 130, 2, 128, seed=40)
+    o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), p["g"].cuda(), H=2, chunk=32)
+    orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], 2)
+    assert rel_err(o.float().cpu(), orf) <= TOL and rel_err(Sf.cpu(), Srf) <= TOL
+    f = torch.randn(1, 130, 2 * 64, generator=torch.Generator().manual_seed(41)).add(2.0)
+    q = torch.randn(1, 130, 2 * 64, generator=torch.Generator().manual_seed(42)) / 8
+    k = torch.randn(1, 130, 2 * 64, generator=torch.Generator().manual_seed(43)) / 8
+    v = torch.randn(1, 130, 2 * 64, generator=torch.Generator().manual_seed(44)) / 8
+    o, Sf = lr.hgrn2(q.cuda(), k.cuda(), v.cuda(), f.cuda(), H=2, gate_lb=0.3)
+    gate = 0.3 + 0.7 * torch.sigmoid(f.double())
+    orf, Srf = oracle.hgrn2(q, k, v, gate, 2)
+    assert rel_err(o.cpu(), orf) <= 1e-4 and rel_err(Sf.cpu(), Srf) <= 1e-4
+
+
+def test_hgrn2_general_path_fast_decay_has_no_range_limit(lr):
+    """Gates of 0.1 (the tensor-core path reports LR_ERR_RANGE) are fine on the
+    step-by-step kernel."""
+    p = general_inputs(1, 128, 1, 64, 64, seed=45, dtype=torch.float32)
+    p["g"] = torch.full_like(p["g"], 0.1)
+    o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), p["g"].cuda(), H=1)
+    torch.cuda.synchronize()
+    assert lr.lr_check_status(0) == 0
+    orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], 1)
+    assert rel_err(o.cpu(), orf) <= 1e-4 and rel_err(Sf.cpu(), Srf) <= 1e-4
