@@ -626,7 +626,7 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
     constexpr int OWN = C::OWN;
     const unsigned FULL = 0xffffffffu;
     const int g0 = lane & ~(LPC - 1);   // first lane of this channel's group
-#pragma unroll 1
+#pragma unroll 2   // two batches in flight: the next batch's softplus overlaps this one's updates
     for (int j0 = 0; j0 < C::T; j0 += C::BATCH) {
         float xv[OWN], dl[OWN], u[OWN];
 #pragma unroll
