@@ -334,3 +334,23 @@ __device__ __forceinline__ void tmem_ld_wait_tied(float (&a)[16], float (&b)[16]
         : "memory");
 }
 }  // namespace lr
+
+namespace lr {
+// Warp-wide TMEM load of the 16-lane, two-half shape: threads 0..15 receive
+// lanes 0..15 of the warp's quarter at columns [c, c + 16), threads 16..31
+// the same lanes at columns [c + split, c + split + 16).  The shape for
+// M = 64 accumulators, whose rows occupy lanes 0..15 of each quarter.
+template <int SPLIT>
+__device__ __forceinline__ void tmem_ld16x2_nowait(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16], %17;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr), "n"(SPLIT));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+}  // namespace lr

@@ -465,22 +465,26 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             if (named_bar_or(1, 32 * KW, !ok)) break;
             tc_fence_after();
             write_state();
-            {   // outputs: o_t = 2^(Lambda_t - m) (OI_t + 2^m OX_t), row t = 16 warp + lane
-                const int t = 16 * warp + lane;
+            {   // outputs: o_t = 2^(Lambda_t - m) (OI_t + 2^m OX_t); the M = 64 rows sit in
+                // lanes 0..15 of the quarter, so the two half-warps take row
+                // t = 16 warp + lane % 16 at columns [16 hh, +16) and [32 + 16 hh, +16)
+                const int t = 16 * warp + (lane & 15);
+                const int cb = 32 * (lane >> 4);
                 const float *e1 = E1 + bi * (C * RB);
                 const float *em = EM + bi * RB;
-                const bool store = lane < 16 && c * C + t < L;
+                const bool store = c * C + t < L;
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {   // 16 value rows i at a time
+                for (int hh = 0; hh < 2; ++hh) {
                     float oi[16], ox[16];
-                    tmem_ld16_nowait(tmem + T_OI + bi * 64 + 16 * hh + lanes, oi);
-                    tmem_ld16_nowait(tmem + T_OX + bi * 64 + 16 * hh + lanes, ox);
+                    tmem_ld16x2_nowait<32>(tmem + T_OI + bi * 64 + 16 * hh + lanes, oi);
+                    tmem_ld16x2_nowait<32>(tmem + T_OX + bi * 64 + 16 * hh + lanes, ox);
                     tmem_ld_wait_tied(oi, ox);
                     if (store) {
+                        const int ib = cb + 16 * hh;
                         uint32_t w[8];
 #pragma unroll
                         for (int q = 0; q < 16; q += 4) {
-                            const int i0 = 16 * hh + q;
+                            const int i0 = ib + q;
                             const float4 e = *reinterpret_cast<const float4 *>(e1 + e1_index(t, i0));
                             const float4 mm = *reinterpret_cast<const float4 *>(em + i0);
                             w[q / 2] = pack_bf16(fmaf(mm.x, ox[q], oi[q]) * e.x,
@@ -489,7 +493,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                                                      fmaf(mm.w, ox[q + 3], oi[q + 3]) * e.w);
                         }
                         uint4 *dst = reinterpret_cast<uint4 *>(o + (size_t(b) * L + c * C + t) * HV +
-                                                               vcol + 16 * hh);
+                                                               vcol + ib);
                         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                     }
