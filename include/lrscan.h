@@ -306,6 +306,12 @@ int lr_rglru_scan_step(const void *x, const void *r, const void *i,
                        float *h_out, void *y, int64_t B, int64_t D,
                        lr_dtype io, lr_stream_t stream);
 
+/* MinMax ([MINMAX] MinMaxNeuron, one token): x = max(min(r, x), s), y = x.
+ * r, s, y: (B, D) io; x_in (NULL = zero), x_out: (B, D) fp32. */
+int lr_minmax_scan_step(const void *r, const void *s, const float *x_in,
+                        float *x_out, void *y, int64_t B, int64_t D, lr_dtype io,
+                        lr_stream_t stream);
+
 int lr_hgrn2_step(const void *q, const void *k, const void *v, const void *g,
                   const float *S_in, float *S_out, void *o,
                   int64_t B, int64_t H, int64_t dk, int64_t dv, lr_dtype io,

@@ -59,6 +59,7 @@ SIGNATURES = {
                                     _I64, _I64, _I64, _I, _I, _P]),
     "lr_rglru_scan_step": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _I64, _I64, _I, _P]),
     "lr_hgrn2_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _P]),
+    "lr_minmax_scan_step": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _P]),
 }
 
 
@@ -179,6 +180,10 @@ def lr_selective_scan_step(x, dt, z, Bm, Cm, A_log, Dskip, h_in, h_out, y, B, D,
 def lr_rglru_scan_step(x, r, i, a_log, c, h_in, h_out, y, B, D, io, stream) -> int:
     return int(_lib.lr_rglru_scan_step(x, r, i, a_log, c, h_in, h_out, y, B, D, io,
                                        stream))
+
+
+def lr_minmax_scan_step(r, s, x_in, x_out, y, B, D, io, stream) -> int:
+    return int(_lib.lr_minmax_scan_step(r, s, x_in, x_out, y, B, D, io, stream))
 
 
 def lr_hgrn2_step(q, k, v, g, S_in, S_out, o, B, H, dk, dv, io, stream) -> int:
@@ -428,6 +433,21 @@ def rglru_scan_step(x, r, i, a_log, c: float = 8.0, h=None, h_out=None):
     _check(lr_rglru_scan_step(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c), _ptr(h_in),
                               _ptr(h_new), _ptr(y), B, D, _io_of(x), stream), "lr_rglru_scan_step")
     return y, h_new
+
+
+def minmax_scan_step(r, s, x=None, x_out=None):
+    """One decode step of the MinMax recurrence.  r, s: (B, D) on the GPU;
+    x: (B, D) fp32 or None (zero).  Returns (y (B, D), x_new (B, D) fp32)."""
+    dev = _target_device(r)
+    r, s = (_dev(t, dev) for t in (r, s))
+    _same(r, s)
+    B, D = r.shape
+    x_in, x_new = _step_state(x, (B, D), dev, x_out)
+    y = torch.empty_like(r)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(lr_minmax_scan_step(_ptr(r), _ptr(s), _ptr(x_in), _ptr(x_new), _ptr(y), B, D, _io_of(r),
+                               stream), "lr_minmax_scan_step")
+    return y, x_new
 
 
 def hgrn2_step(q, k, v, g, H: int, S=None, S_out=None):

@@ -363,3 +363,16 @@ extern "C" int lr_hgrn2_preact_fwd(const void *q, const void *k, const void *v, 
                                         true, lb, st);
     return lr::hgrn2_launch(q, k, v, f, S0, o, S_final, B, L, H, workspace, st, true, lb);
 }
+
+extern "C" int lr_minmax_scan_step(const void *r, const void *s, const float *x_in, float *x_out,
+                                   void *y, int64_t B, int64_t D, lr_dtype io, lr_stream_t stream) {
+    if (B < 0 || D < 0 || !io_ok(io)) return LR_ERR_INVALID_ARG;
+    if (B * D > 0) {
+        const void *req[] = {r, s, x_out, y};
+        const void *all[] = {r, s, x_in, x_out, y};
+        const int rc = validate_step_common(req, 4, all, 5);
+        if (rc != LR_OK) return rc;
+    }
+    return lr::minmax_step_launch(r, s, x_in, x_out, y, B, D, io == LR_BF16,
+                                  reinterpret_cast<cudaStream_t>(stream));
+}

@@ -77,6 +77,8 @@ int selective_step_launch(const void *x, const void *dt, const void *z, const vo
 int rglru_step_launch(const void *x, const void *r, const void *i, const float *a_log, float c,
                       const float *h_in, float *h_out, void *y, int64_t B, int64_t D, int io_bf16,
                       cudaStream_t stream);
+int minmax_step_launch(const void *r, const void *s, const float *x_in, float *x_out, void *y,
+                       int64_t B, int64_t D, int io_bf16, cudaStream_t stream);
 int hgrn2_step_launch(const void *q, const void *k, const void *v, const void *g, const float *S_in,
                       float *S_out, void *o, int64_t B, int64_t H, int64_t dk, int64_t dv, int io_bf16,
                       cudaStream_t stream);

@@ -85,6 +85,22 @@ __global__ void __launch_bounds__(kStepThreads)
     y[idx] = Io<IO>::from_f(h);
 }
 
+// MinMax, one thread per (b, d): x = max(min(r, x), s); y = x.  min.NaN /
+// max.NaN propagate NaN like torch.minimum / torch.maximum.
+template <typename IO>
+__global__ void __launch_bounds__(kStepThreads)
+    minmax_step_kernel(const IO *__restrict__ r, const IO *__restrict__ s, const float *x_in,
+                       float *x_out, IO *__restrict__ y, int64_t B, int64_t D) {
+    const int64_t idx = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
+    if (idx >= B * D) return;
+    float x = x_in != nullptr ? x_in[idx] : 0.0f;
+    float lo;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(lo) : "f"(Io<IO>::to_f(r[idx])), "f"(x));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(x) : "f"(lo), "f"(Io<IO>::to_f(s[idx])));
+    x_out[idx] = x;
+    y[idx] = Io<IO>::from_f(x);
+}
+
 // Four consecutive elements as fp32 (16-byte fp32 or 8-byte bf16 load).
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 __device__ __forceinline__ float4 ld4(const __nv_bfloat16 *p) {
@@ -210,6 +226,21 @@ int hgrn2_step_launch(const void *q, const void *k, const void *v, const void *g
                                        static_cast<const float *>(v), static_cast<const float *>(g),
                                        S_in, S_out, static_cast<float *>(o), B, H, dk, dv);
     }
+    return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+}
+
+int minmax_step_launch(const void *r, const void *s, const float *x_in, float *x_out, void *y,
+                       int64_t B, int64_t D, int io_bf16, cudaStream_t stream) {
+    if (B * D == 0) return LR_OK;
+    const unsigned grid = blocks_for(B * D, kStepThreads);
+    if (io_bf16)
+        minmax_step_kernel<__nv_bfloat16><<<grid, kStepThreads, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(r), static_cast<const __nv_bfloat16 *>(s), x_in, x_out,
+            static_cast<__nv_bfloat16 *>(y), B, D);
+    else
+        minmax_step_kernel<float><<<grid, kStepThreads, 0, stream>>>(
+            static_cast<const float *>(r), static_cast<const float *>(s), x_in, x_out,
+            static_cast<float *>(y), B, D);
     return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 

@@ -239,3 +239,11 @@ def test_rglru_preact_validation_matches_plain(lr):
     assert lr.lr_rglru_scan_preact_fwd(*a.values()) == lr.LR_ERR_INVALID_ARG
     a = rg_args(D=12)
     assert lr.lr_rglru_scan_preact_fwd(*a.values()) == lr.LR_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,code", [(dict(r=None), -1), (dict(x_out=None), -1), (dict(B=-1), -1),
+                                     (dict(x_in=FAKE + 4), -3)])
+def test_minmax_step_validation_codes(lr, kw, code):
+    a = dict(r=FAKE, s=FAKE, x_in=FAKE, x_out=FAKE, y=FAKE, B=2, D=64, io=1, stream=None)
+    a.update(kw)
+    assert lr.lr_minmax_scan_step(*a.values()) == code

@@ -115,3 +115,18 @@ def test_step_zero_state_equals_explicit_zeros(lr):
     y1, h1 = lr.rglru_scan_step(d["x"][:, 0], d["r"][:, 0], d["i"][:, 0], d["a_log"], d["c"],
                                 h=torch.zeros(2, 64, device="cuda"))
     assert torch.equal(y0, y1) and torch.equal(h0, h1)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_minmax_steps_equal_the_scan_bit_for_bit(lr, io):
+    """Chained in-place MinMax steps reproduce the oracle's sequence exactly."""
+    dt = torch.float32 if io == "f32" else torch.bfloat16
+    g = torch.Generator().manual_seed(38)
+    r = torch.randn(2, 25, 64, generator=g).to(dt)
+    s = (torch.randn(2, 25, 64, generator=g) - 1).to(dt)
+    x0 = torch.randn(2, 64, generator=g).to(dt).float()
+    x = x0.cuda()
+    ys = [lr.minmax_scan_step(r[:, t].cuda(), s[:, t].cuda(), x=x, x_out=x)[0] for t in range(25)]
+    yr, xr = oracle.minmax_scan(r, s, x0)
+    assert np.array_equal(torch.stack(ys, 1).double().cpu().numpy(), yr)
+    assert np.array_equal(x.double().cpu().numpy(), xr)
