@@ -489,7 +489,7 @@ def gpu_arm(args):
         "gpu_launches": len(cfgs) * args.steps,
         "clocks": clk,
     }
-    if not args.seq_len and not args.only:
+    if not args.seq_len and not args.only and not args.no_extras:
         line["decode"] = decode_timings(lr, cfgs, dev)
         line["extra"] = extra_timings(lr, dev, peaks)
     if rank == 0 and not args.no_cpu_baseline:
@@ -587,6 +587,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the CPU oracle beside the GPU arm")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the decode-step and extra-scan timings after the step")
     ap.add_argument("--only", choices=["rglru", "selective", "hgrn2"], default=None,
                     help="run one scan of the step (profiling case)")
     ap.add_argument("--seq-len", type=int, default=None,
