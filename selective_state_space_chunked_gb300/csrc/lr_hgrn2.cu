@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             mbar_init(&fdone[k], 1);
             mbar_init(&kdone[k], KW);
         }
-        mbar_init(sbready, 1);
+        mbar_init(sbready, KW);   // each back warp publishes its own 32 rows
         mbar_init(mma_done, 2);
         *abort_flag = 0;
         fence_mbar_init();
@@ -412,7 +412,11 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             }
         }
     } else {  // ------------------------------------------------------------ back
-        // key column j = tid of value rows rb*64 .. rb*64+63 of S[b, h]
+        // key column j = tid of value rows rb*64 .. rb*64+63 of S[b, h].  The
+        // four back warps share no data: each publishes the bf16 rows of its
+        // own 32 keys and releases its own TMEM lanes, so they run without a
+        // block barrier and the abort decision is taken per warp.
+        const unsigned FULLM = 0xffffffffu;
         const size_t srow0 = size_t(bh) * DV + size_t(rb) * RB;
         float S[RB];
 #pragma unroll
@@ -425,16 +429,21 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                     make_uint4(pack_bf16(S[8 * k], S[8 * k + 1]), pack_bf16(S[8 * k + 2], S[8 * k + 3]),
                                pack_bf16(S[8 * k + 4], S[8 * k + 5]), pack_bf16(S[8 * k + 6], S[8 * k + 7]));
             fence_proxy_async_smem();
-            named_bar(1, 32 * KW);
-            if (tid == 0) arrive(sbready);
+            __syncwarp();
+            if (lane == 0) arrive(sbready);
         };
         write_state();
         const uint32_t lanes = uint32_t(warp * 32) << 16;
+        // o_t = 2^(Lambda_t - m) (OI_t + 2^m OX_t); the M = 64 rows sit in lanes
+        // 0..15 of the quarter, so the two half-warps take row t = 16 warp +
+        // lane % 16 at columns [16 hh, +16) and [32 + 16 hh, +16)
+        const int t = 16 * warp + (lane & 15);
+        const int cb = 32 * (lane >> 4);
         for (int c = 0; c < n_chunks; ++c) {
             const int bi = c & 1;
             bool ok = hw(&fdone[bi], (c >> 1) & 1);
             if (ok) ok = hw(&bar_o[bi], (c >> 1) & 1);
-            if (named_bar_or(1, 32 * KW, !ok)) break;
+            if (!__all_sync(FULLM, ok)) break;
             tc_fence_after();
             {   // S = diag(2^Lambda_C) S + dS   (dS^T lane j, column i)
                 const float *gc = GC + bi * RB;
@@ -462,41 +471,40 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             }
             // OX_c reads the previous bf16 state until bar_x
             ok = hw(&bar_x[bi], (c >> 1) & 1);
-            if (named_bar_or(1, 32 * KW, !ok)) break;
+            if (!__all_sync(FULLM, ok)) break;
             tc_fence_after();
+            // the first output columns' accumulator loads overlap the state write
+            float oi[16], ox[16];
+            tmem_ld16x2_nowait<32>(tmem + T_OI + bi * 64 + lanes, oi);
+            tmem_ld16x2_nowait<32>(tmem + T_OX + bi * 64 + lanes, ox);
             write_state();
-            {   // outputs: o_t = 2^(Lambda_t - m) (OI_t + 2^m OX_t); the M = 64 rows sit in
-                // lanes 0..15 of the quarter, so the two half-warps take row
-                // t = 16 warp + lane % 16 at columns [16 hh, +16) and [32 + 16 hh, +16)
-                const int t = 16 * warp + (lane & 15);
-                const int cb = 32 * (lane >> 4);
-                const float *e1 = E1 + bi * (C * RB);
-                const float *em = EM + bi * RB;
-                const bool store = c * C + t < L;
+            const float *e1 = E1 + bi * (C * RB);
+            const float *em = EM + bi * RB;
+            const bool store = c * C + t < L;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float oi[16], ox[16];
+            for (int hh = 0; hh < 2; ++hh) {
+                if (hh > 0) {
                     tmem_ld16x2_nowait<32>(tmem + T_OI + bi * 64 + 16 * hh + lanes, oi);
                     tmem_ld16x2_nowait<32>(tmem + T_OX + bi * 64 + 16 * hh + lanes, ox);
-                    tmem_ld_wait_tied(oi, ox);
-                    if (store) {
-                        const int ib = cb + 16 * hh;
-                        uint32_t w[8];
+                }
+                tmem_ld_wait_tied(oi, ox);
+                if (store) {
+                    const int ib = cb + 16 * hh;
+                    uint32_t w[8];
 #pragma unroll
-                        for (int q = 0; q < 16; q += 4) {
-                            const int i0 = ib + q;
-                            const float4 e = *reinterpret_cast<const float4 *>(e1 + e1_index(t, i0));
-                            const float4 mm = *reinterpret_cast<const float4 *>(em + i0);
-                            w[q / 2] = pack_bf16(fmaf(mm.x, ox[q], oi[q]) * e.x,
-                                                 fmaf(mm.y, ox[q + 1], oi[q + 1]) * e.y);
-                            w[q / 2 + 1] = pack_bf16(fmaf(mm.z, ox[q + 2], oi[q + 2]) * e.z,
-                                                     fmaf(mm.w, ox[q + 3], oi[q + 3]) * e.w);
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(o + (size_t(b) * L + c * C + t) * HV +
-                                                               vcol + ib);
-                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int q = 0; q < 16; q += 4) {
+                        const int i0 = ib + q;
+                        const float4 e = *reinterpret_cast<const float4 *>(e1 + e1_index(t, i0));
+                        const float4 mm = *reinterpret_cast<const float4 *>(em + i0);
+                        w[q / 2] = pack_bf16(fmaf(mm.x, ox[q], oi[q]) * e.x,
+                                             fmaf(mm.y, ox[q + 1], oi[q + 1]) * e.y);
+                        w[q / 2 + 1] = pack_bf16(fmaf(mm.z, ox[q + 2], oi[q + 2]) * e.z,
+                                                 fmaf(mm.w, ox[q + 3], oi[q + 3]) * e.w);
                     }
+                    uint4 *dst = reinterpret_cast<uint4 *>(o + (size_t(b) * L + c * C + t) * HV +
+                                                           vcol + ib);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
             tc_fence_before();
