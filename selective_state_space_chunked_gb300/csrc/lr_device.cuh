@@ -354,3 +354,15 @@ __device__ __forceinline__ void tmem_ld16x2_nowait(uint32_t taddr, float (&v)[16
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 }  // namespace lr
+
+namespace lr {
+__device__ __forceinline__ void tmem_ld_wait_tied(float (&a)[16]) {
+    asm volatile(
+        "tcgen05.wait::ld.sync.aligned;"
+        : "+f"(a[0]), "+f"(a[1]), "+f"(a[2]), "+f"(a[3]), "+f"(a[4]), "+f"(a[5]), "+f"(a[6]),
+          "+f"(a[7]), "+f"(a[8]), "+f"(a[9]), "+f"(a[10]), "+f"(a[11]), "+f"(a[12]), "+f"(a[13]),
+          "+f"(a[14]), "+f"(a[15])
+        :
+        : "memory");
+}
+}  // namespace lr

@@ -316,7 +316,6 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             // inputs landed; 2^(Lambda - m) buffer free (back done with chunk c-2)
             bool ok = hw(&full[st], (c / NST) & 1);
             if (ok && c >= 2) ok = hw(&kdone[bi], ((c - 2) >> 1) & 1);
-            if (named_bar_or(2, 32 * FW, !ok)) break;
 
             // cumulative log2 gates over this thread's steps (steps past L: g = 1)
             const int t0 = c * C;
@@ -332,7 +331,9 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             }
             TOTF[qt * RB + i] = acc;
             if (qt == 0) L0F[i] = loc[0];
-            named_bar(2, 32 * FW);
+            // the quarter totals are exchanged here; a failed wait anywhere ends
+            // the loop for every front thread together
+            if (named_bar_or(2, 32 * FW, !ok)) break;
             float off = 0.0f, lc = 0.0f;
 #pragma unroll
             for (int q = 0; q < FQ; ++q) {
@@ -352,21 +353,23 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                 EM[bi * RB + i] = ex2_approx(m);
                 GC[bi * RB + i] = ex2_approx(lc);
             }
-            {   // V~ = 2^(m - Lambda) v and V~' = 2^(Lambda_C - m) V~ for row i, these steps
-                const float cm = ex2_approx(lc - m);
-                uint32_t vt[FSTEPS / 2], vtp[FSTEPS / 2];
+            // V~ = 2^(m - Lambda) v and V~' = 2^(Lambda_C - m) V~ for row i, these steps
+            const float cm = ex2_approx(lc - m);
+            uint32_t vt[FSTEPS / 2], vtp[FSTEPS / 2];
 #pragma unroll
-                for (int u = 0; u < FSTEPS; u += 2) {
-                    const int t = tb + u;
-                    const float w0 = ex2_approx(m - loc[u]) * __bfloat162float(sV[t * RB + i]);
-                    const float w1 = ex2_approx(m - loc[u + 1]) * __bfloat162float(sV[(t + 1) * RB + i]);
-                    vt[u / 2] = pack_bf16(w0, w1);
-                    vtp[u / 2] = pack_bf16(w0 * cm, w1 * cm);
-                }
-                // the V~, V~' and masked-P buffers are free once dS and OI of
-                // chunk c-1 completed; the work above overlapped with them
-                ok = c == 0 || hw(&bar_o[(c - 1) & 1], ((c - 1) >> 1) & 1);
-                if (named_bar_or(2, 32 * FW, !ok)) break;
+            for (int u = 0; u < FSTEPS; u += 2) {
+                const int t = tb + u;
+                const float w0 = ex2_approx(m - loc[u]) * __bfloat162float(sV[t * RB + i]);
+                const float w1 = ex2_approx(m - loc[u + 1]) * __bfloat162float(sV[(t + 1) * RB + i]);
+                vt[u / 2] = pack_bf16(w0, w1);
+                vtp[u / 2] = pack_bf16(w0 * cm, w1 * cm);
+            }
+            // the V~, V~' and masked-P buffers are free once dS and OI of chunk
+            // c-1 completed (the work above overlapped with them); P_c is ready
+            ok = c == 0 || hw(&bar_o[(c - 1) & 1], ((c - 1) >> 1) & 1);
+            if (ok) ok = hw(&bar_p[bi], (c >> 1) & 1);
+            ok = __all_sync(0xffffffffu, ok);   // the TMEM load below is warp-collective
+            if (ok) {
 #pragma unroll
                 for (int k = 0; k < FSTEPS / 8; ++k) {
                     const uint32_t o8 = sw128_offset(i, tb + 8 * k);
@@ -375,37 +378,34 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                     *reinterpret_cast<uint4 *>(VTP + o8) =
                         make_uint4(vtp[4 * k], vtp[4 * k + 1], vtp[4 * k + 2], vtp[4 * k + 3]);
                 }
-            }
-            // causal mask of P_c: M = 64 rows t sit in lanes 0..15 of each warp
-            // quarter; the two warps of a quarter take 32 columns s each
-            ok = hw(&bar_p[bi], (c >> 1) & 1);
-            if (named_bar_or(2, 32 * FW, !ok)) break;
-            tc_fence_after();
-            {
-                const int quarter = fw & 3, s_base = 32 * (fw >> 2);
-                float pv[32];
-                tmem_ld32_nowait(tmem + T_P + bi * 64 + s_base + (uint32_t(quarter * 32) << 16), pv);
+                // causal mask of P_c: the M = 64 rows t sit in lanes 0..15 of each
+                // warp quarter; the two warps of a quarter take 32 columns s each,
+                // their half-warps 16 columns each (two-half TMEM load)
+                tc_fence_after();
+                const int quarter = fw & 3;
+                const int s_base = 32 * (fw >> 2) + 16 * (lane >> 4);
+                float pv[16];
+                tmem_ld16x2_nowait<16>(tmem + T_P + bi * 64 + 32 * (fw >> 2) +
+                                           (uint32_t(quarter * 32) << 16), pv);
                 tmem_ld_wait_tied(pv);
-                const int t = 16 * quarter + lane;
-                if (lane < 16) {
+                const int t = 16 * quarter + (lane & 15);
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t w4[4];
+                for (int ch = 0; ch < 2; ++ch) {
+                    uint32_t w4[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int s0 = s_base + ch * 8 + 2 * e;
-                            w4[e] = pack_bf16(s0 <= t ? pv[ch * 8 + 2 * e] : 0.0f,
-                                              s0 + 1 <= t ? pv[ch * 8 + 2 * e + 1] : 0.0f);
-                        }
-                        const int chunk = (s_base >> 3) + ch;
-                        *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) =
-                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const int s0 = s_base + ch * 8 + 2 * e;
+                        w4[e] = pack_bf16(s0 <= t ? pv[ch * 8 + 2 * e] : 0.0f,
+                                          s0 + 1 <= t ? pv[ch * 8 + 2 * e + 1] : 0.0f);
                     }
+                    const int chunk = (s_base >> 3) + ch;
+                    *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar(2, 32 * FW);
+            if (named_bar_or(2, 32 * FW, !ok)) break;
             if (f == 0) {
                 arrive(&fdone[bi]);
                 arrive(&empty[st]);   // V, g of stage st no longer read
