@@ -68,7 +68,7 @@ def algorithmic(cfg: wl.Config) -> dict:
 
 
 # The scans one step runs (the workloads the pages' layers are sized for).
-STEP_CONFIGS = (2, 3, 4)
+STEP_WORKLOADS = ("rglru_bf16", "selective_bf16", "hgrn2_bf16")
 
 
 def step_configs(only=None, seq_len=None):
@@ -76,7 +76,7 @@ def step_configs(only=None, seq_len=None):
     the sequences (profiling cases: a launch of the same kernel on a smaller
     input, never a benchmark number)."""
     import dataclasses
-    cfgs = [wl.CONFIGS[k] for k in STEP_CONFIGS]
+    cfgs = [wl.WORKLOADS[k] for k in STEP_WORKLOADS]
     if only:
         cfgs = [c for c in cfgs if c.form == only]
     if seq_len:
@@ -361,13 +361,13 @@ def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
     del r, s_
     # the RG-LRU and HGRN2 workloads with their gates before the activation
     # (sigmoid / lower-bounded sigmoid applied in the kernel)
-    cfg = wl.CONFIGS[2]
+    cfg = wl.WORKLOADS["rglru_bf16"]
     p = wl.make_inputs(cfg, device=dev)
     res.append(entry(cfg.name + " gates_preact", timed(lambda: lr.rglru_scan(
         p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"], gates_preact=True)),
         cfg.B * cfg.L * cfg.D, algorithmic(cfg)["bytes"]))
     del p
-    cfg = wl.CONFIGS[4]
+    cfg = wl.WORKLOADS["hgrn2_bf16"]
     p = wl.make_inputs(cfg, device=dev)
     res.append(entry(cfg.name + " gate_lb=0.2", timed(lambda: lr.hgrn2(
         p["q"], p["k"], p["v"], p["g"], H=p["H"], gate_lb=0.2)),

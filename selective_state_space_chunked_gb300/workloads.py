@@ -32,7 +32,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "CONFIGS", "Config", "multiscale_A_log", "rglru_inputs",
+    "WORKLOADS", "Config", "multiscale_A_log", "rglru_inputs",
     "selective_inputs", "hgrn2_inputs", "make_inputs",
 ]
 
@@ -69,15 +69,16 @@ class Config:
         return self.B * self.L * self.D
 
 
-# The five workloads the pages' layers are sized for (index = seed).
-CONFIGS = {
-    0: Config(0, "rglru", B=2, L=128, D=64, io="f32", seed=0),
-    1: Config(1, "selective", B=2, L=1024, D=1536, io="f32", seed=1),
-    2: Config(2, "rglru", B=8, L=4096, D=2560, io="bf16", seed=2, with_h0=True),
-    3: Config(3, "selective", B=4, L=16384, D=4096, io="bf16", seed=3,
-              with_h0=True),
-    4: Config(4, "hgrn2", B=4, L=4096, D=2048, io="bf16", seed=4, H=16,
-              head_dim=128),
+# The five workloads the pages' layers are sized for, by name (the index is
+# the seed).
+WORKLOADS = {
+    "rglru_f32_small": Config(0, "rglru", B=2, L=128, D=64, io="f32", seed=0),
+    "selective_f32": Config(1, "selective", B=2, L=1024, D=1536, io="f32", seed=1),
+    "rglru_bf16": Config(2, "rglru", B=8, L=4096, D=2560, io="bf16", seed=2, with_h0=True),
+    "selective_bf16": Config(3, "selective", B=4, L=16384, D=4096, io="bf16", seed=3,
+                             with_h0=True),
+    "hgrn2_bf16": Config(4, "hgrn2", B=4, L=4096, D=2048, io="bf16", seed=4, H=16,
+                         head_dim=128),
 }
 
 

@@ -62,9 +62,9 @@ def check_rglru(lr, p, io):
     return y, hf
 
 
-def test_rglru_config0_page_example(lr):
+def test_rglru_small_f32_page_example(lr):
     """B=2, L=128, D=64, fp32 (the page's (2,128,64) -> (2,128,64) example)."""
-    cfg = wl.CONFIGS[0]
+    cfg = wl.WORKLOADS["rglru_f32_small"]
     p = wl.make_inputs(cfg)
     y, hf = check_rglru(lr, p, "f32")
     assert y.shape == (2, 128, 64) and hf.shape == (2, 64)
@@ -75,7 +75,7 @@ def test_rglru_config0_page_example(lr):
     (3, 257, 72, "bf16", False),     # D not a multiple of the 64-channel block
     (1, 1, 64, "f32", True),         # single step
     (2, 33, 12, "f32", True),        # tiny ragged everything
-    (4, 640, 2560, "bf16", True),    # the large config's channel width
+    (4, 640, 2560, "bf16", True),    # the RG-LRU workload's channel width
 ])
 def test_rglru_oracle_sized(lr, B, L, D, io, h0):
     p = wl.rglru_inputs(B, L, D, seed=B * 1000 + L, io=io, with_h0=h0)
@@ -114,9 +114,9 @@ def test_rglru_zero_length_returns_initial_state(lr):
     assert torch.equal(hf, p["h0"])
 
 
-def test_rglru_config2_full_size_sampled(lr):
+def test_rglru_bf16_B8_L4096_D2560_sampled(lr):
     """B=8, L=4096, D=2560, bf16 I/O, h0 ~ N(0,1): the benchmark's launch."""
-    cfg = wl.CONFIGS[2]
+    cfg = wl.WORKLOADS["rglru_bf16"]
     p = wl.make_inputs(cfg, device="cuda")
     y, hf = lr.rglru_scan(p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"])
     torch.cuda.synchronize()
@@ -151,9 +151,9 @@ def check_sel(lr, p, io, **over):
     assert rel_err(hf, hr) <= TOL[io], rel_err(hf, hr)
 
 
-def test_selective_config1_full(lr):
+def test_selective_f32_B2_L1024_D1536_full(lr):
     """B=2, L=1024, d_inner=1536 (4 scales of 384), N=16, fp32 I/O."""
-    p = wl.make_inputs(wl.CONFIGS[1])
+    p = wl.make_inputs(wl.WORKLOADS["selective_f32"])
     check_sel(lr, p, "f32")
 
 
@@ -162,7 +162,7 @@ def test_selective_config1_full(lr):
     (3, 97, 40, "bf16", False),      # D not a multiple of the 32-channel block
     (1, 1, 32, "f32", True),
     (2, 45, 8, "f32", True),
-    (1, 333, 4096, "bf16", True),    # the long-sequence config's width
+    (1, 333, 4096, "bf16", True),    # the selective workload's channel width
 ])
 def test_selective_oracle_sized(lr, B, L, D, io, h0):
     p = wl.selective_inputs(B, L, D, seed=B + L + D, io=io, with_h0=h0)
@@ -186,10 +186,10 @@ def test_selective_forced_time_splits_lookback(lr, splits, io):
     check_sel(lr, p, io)
 
 
-def test_selective_config3_full_size_sampled_and_four_segments(lr):
+def test_selective_bf16_B4_L16384_D4096_sampled_and_four_segments(lr):
     """B=4, L=16384, d_inner=4096, N=16, bf16 I/O, h0 ~ N(0,1); also run as 4
     segments of 4096 carried through the final state."""
-    cfg = wl.CONFIGS[3]
+    cfg = wl.WORKLOADS["selective_bf16"]
     p = wl.make_inputs(cfg, device="cuda")
     args = (p["x"], p["dt"], p["Bm"], p["Cm"], p["A_log"])
     y, hf = lr.selective_scan(*args, z=p["z"], Dskip=p["Dskip"], h0=p["h0"])

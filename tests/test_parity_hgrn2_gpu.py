@@ -89,9 +89,9 @@ def test_hgrn2_gate_spread_beyond_range_is_reported(lr):
     assert lr.lr_check_status(0) == 0
 
 
-def test_hgrn2_config4_full_size_sampled(lr):
+def test_hgrn2_bf16_B4_L4096_H16_sampled(lr):
     """B=4, L=4096, hidden 2048 = 16 heads x 128, bf16, g = 0.2 + 0.8 sigmoid(f)."""
-    cfg = wl.CONFIGS[4]
+    cfg = wl.WORKLOADS["hgrn2_bf16"]
     p = wl.make_inputs(cfg, device="cuda")
     o, Sf = lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=cfg.H)
     torch.cuda.synchronize()
