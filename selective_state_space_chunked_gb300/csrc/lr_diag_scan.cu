@@ -605,8 +605,8 @@ struct SelCfg {
     static constexpr int CWARPS = DC * LPC / 32;
     static constexpr int THREADS = 32 * (CWARPS + 1);    // + producer warp
     static constexpr int N = 16, NS = N / LPC, NP = NS / 2;
-    static constexpr int T = 32;
-    static constexpr int STAGES = 4;
+    static constexpr int T = 64;                         // steps per tile
+    static constexpr int STAGES = 2;                     // 2 x 64 steps in flight (48 KB with the fp32 B/C copies)
     static constexpr int BATCH = 8;
     static constexpr int OWN = BATCH / LPC;              // steps a lane prepares per batch
     static constexpr int TILE = T * DC;                  // x / dt / z tile elements
