@@ -176,10 +176,13 @@ struct BlockAbort {
 template <typename IO>
 struct RgCfg {
     static constexpr int DC = 64;                        // channels per block
-    static constexpr int T = 32;                         // time steps per tile
+    // time steps per tile; bf16 tiles are 64 steps deep in 3 stages (the same
+    // 72 KB as 6 x 32 steps, so 3 blocks stay resident per SM, with half the
+    // handshakes per step)
+    static constexpr int T = sizeof(IO) == 2 ? 64 : 32;
     static constexpr int CWARPS = DC / 32;
     static constexpr int THREADS = 32 * (CWARPS + 1);    // + producer warp
-    static constexpr int STAGES = sizeof(IO) == 2 ? 6 : 4;
+    static constexpr int STAGES = sizeof(IO) == 2 ? 3 : 4;
     static constexpr int BATCH = 8;
     static constexpr int TILE = T * DC;
     static constexpr uint32_t STAGE_BYTES = 3u * TILE * sizeof(IO);
@@ -208,10 +211,22 @@ __device__ __forceinline__ void rglru_ab(float r, float u, float cl, float cl2, 
 // scheduler can interleave), and a ragged output tile.
 enum TileMode { kAggregate = 0, kFull = 1, kRagged = 2 };
 
-// Logistic sigmoid of a pre-activation gate.
+// Logistic sigmoids of both pre-activation gates.  The fast form shares one
+// reciprocal: with e = exp(-v) clamped to 2^60 (so the product stays finite;
+// sigma moves by less than 1e-18), sigma(r) = (1 + e_i) / ((1 + e_r)(1 + e_i))
+// and likewise for i -- five special-function operations per step, not six.
 template <bool ACC>
-__device__ __forceinline__ float sigmoid_t(float v) {
-    return ACC ? 1.0f / (1.0f + expf(-v)) : rcp_approx(1.0f + ex2_approx(-v * kLog2e));
+__device__ __forceinline__ void sigmoid_pair(float &r, float &i) {
+    if (ACC) {
+        r = 1.0f / (1.0f + expf(-r));
+        i = 1.0f / (1.0f + expf(-i));
+    } else {
+        const float er1 = 1.0f + fminf(ex2_approx(-r * kLog2e), 0x1p60f);
+        const float ei1 = 1.0f + fminf(ex2_approx(-i * kLog2e), 0x1p60f);
+        const float inv = rcp_approx(er1 * ei1);
+        r = ei1 * inv;
+        i = er1 * inv;
+    }
 }
 
 // One T-step tile of one channel's recurrence.  PRE: r and i arrive before
@@ -221,17 +236,18 @@ template <typename IO, bool ACC, bool PRE, int MODE>
 __device__ __forceinline__ void rglru_tile(const IO *xs, const IO *rs, const IO *is, float cl,
                                            float cl2, float &h, float &P, IO *yp, int D, int rows) {
     using C = RgCfg<IO>;
-#pragma unroll
+    // the whole tile unrolled keeps every batch's loads ahead of the chain;
+    // with the two sigmoids per step that would take 191 registers, so the
+    // pre-activation form unrolls four batches (96 registers)
+    constexpr int kUnroll = PRE ? 4 : C::T / C::BATCH;
+#pragma unroll kUnroll
     for (int j0 = 0; j0 < C::T; j0 += C::BATCH) {
         float a[C::BATCH], bb[C::BATCH];
 #pragma unroll
         for (int u = 0; u < C::BATCH; ++u) {
             const int o = (j0 + u) * C::DC;
             float rv = Io<IO>::to_f(rs[o]), iv = Io<IO>::to_f(is[o]);
-            if (PRE) {
-                rv = sigmoid_t<ACC>(rv);
-                iv = sigmoid_t<ACC>(iv);
-            }
+            if (PRE) sigmoid_pair<ACC>(rv, iv);
             rglru_ab<ACC>(rv, iv * Io<IO>::to_f(xs[o]), cl, cl2, a[u], bb[u]);
             // rows past L arrive zero-filled; with raw gates r = 0 is the
             // identity step (a = 1, b = 0), after a sigmoid it is not
@@ -1109,7 +1125,7 @@ int rglru_plan(int64_t B, int64_t L, int64_t D, lr_dtype io, DiagPlan *p) {
     if (device_sm_count(&sms) != LR_OK || current_device(&dev) != LR_OK) return LR_ERR_CUDA;
     *p = DiagPlan{};
     p->dc = RgCfg<float>::DC;
-    p->tile_t = RgCfg<float>::T;
+    p->tile_t = io == LR_BF16 ? RgCfg<__nv_bfloat16>::T : RgCfg<float>::T;
     p->n_cb = B * ((D + p->dc - 1) / p->dc);
     p->n_tiles = static_cast<int>((L + p->tile_t - 1) / p->tile_t);
     const int per_sm = io == LR_BF16 ? rglru_resident<__nv_bfloat16, false>(dev)

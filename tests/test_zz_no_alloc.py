@@ -67,14 +67,15 @@ def test_noalloc_matches_workspace_entry_two_calls(lr, io):
 
 def test_noalloc_rejects_problems_beyond_builtin_scratch(lr):
     p = {k: (v.cuda() if torch.is_tensor(v) else v)
-         for k, v in wl.rglru_inputs(4, 4096, 256, seed=1, io="bf16").items()}
-    prev = lr.lr_set_split_override(128)   # 16 blocks x 128 splits: ~1.6 MB of scratch
+         for k, v in wl.rglru_inputs(4, 8192, 256, seed=1, io="bf16").items()}
+    # 16 blocks x 128 splits (one 64-step tile each): ~1.6 MB of scratch
+    prev = lr.lr_set_split_override(128)
     try:
-        assert lr.lr_rglru_scan_workspace_size(4, 4096, 256, lr.LR_BF16) > (1 << 20)
+        assert lr.lr_rglru_scan_workspace_size(4, 8192, 256, lr.LR_BF16) > (1 << 20)
         y = torch.empty_like(p["x"])
         rc = lr.lr_rglru_scan_fwd_noalloc(
             p["x"].data_ptr(), p["r"].data_ptr(), p["i"].data_ptr(), p["a_log"].data_ptr(),
-            8.0, None, y.data_ptr(), None, 4, 4096, 256, lr.LR_BF16,
+            8.0, None, y.data_ptr(), None, 4, 8192, 256, lr.LR_BF16,
             torch.cuda.current_stream().cuda_stream)
         assert rc == lr.LR_ERR_WORKSPACE
     finally:
