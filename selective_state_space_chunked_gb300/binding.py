@@ -335,8 +335,8 @@ def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None
           sync_host: bool = True, gate_lb: Optional[float] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """HGRN2 matrix-state recurrence.  q, k: (B, L, H*dk); v, g: (B, L, H*dv)
     (g after its activation and lower bound; with ``gate_lb`` set, g is the
-    pre-activation f and the kernel forms lb + (1 - lb) sigmoid(f)),
-    bfloat16; S0: (B, H, dv, dk) fp32.  Returns (o (B, L, H*dv), S_final
+    pre-activation f and the kernel forms lb + (1 - lb) sigmoid(f)), one
+    dtype (bfloat16 or float32); S0: (B, H, dv, dk) fp32.  Returns (o (B, L, H*dv), S_final
     (B, H, dv, dk) fp32); ``out=(o, S_final)`` gives the result tensors (GPU
     or host).  Raises ValueError when the hidden size is not divisible by
     the head count."""

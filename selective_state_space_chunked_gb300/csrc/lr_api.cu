@@ -141,10 +141,11 @@ int lr_version(void) { return kVersion; }
 int lr_check_status(lr_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return LR_ERR_CUDA;
-    int s1 = 0, s2 = 0;
+    int s1 = 0, s2 = 0, s3 = 0;
     if (lr::diag_status_read_and_clear(&s1) != LR_OK) return LR_ERR_CUDA;
     if (lr::hgrn2_status_read_and_clear(&s2) != LR_OK) return LR_ERR_CUDA;
-    return s1 != 0 ? s1 : s2;
+    if (lr::hgrn2_general_status_read_and_clear(&s3) != LR_OK) return LR_ERR_CUDA;
+    return s1 != 0 ? s1 : (s2 != 0 ? s2 : s3);
 }
 
 int lr_set_split_override(int splits) {

@@ -995,19 +995,27 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D map over a row-major (d2, d1, d0) tensor, box (b0, b1, 1), no swizzle,
-// zero fill outside the tensor.
-bool make_map_3d(CUtensorMap *tm, const void *base, CUtensorMapDataType type, size_t esize,
-                 uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+}  // namespace
+
+bool encode_map_3d(CUtensorMap *tm, const void *base, CUtensorMapDataType type, size_t esize,
+                   uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[3] = {d0, d1, d2};
     const cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
-    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(tm, type, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
+// 3-D map over a row-major (d2, d1, d0) tensor, box (b0, b1, 1).
+bool make_map_3d(CUtensorMap *tm, const void *base, CUtensorMapDataType type, size_t esize,
+                 uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+    return encode_map_3d(tm, base, type, esize, d0, d1, d2, b0, b1, 1);
 }
 
 // Per-device facts and per-kernel attributes, looked up once.

@@ -4,6 +4,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "lrscan.h"
@@ -65,6 +66,13 @@ int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, con
                  cudaStream_t stream, bool preact = false, float lb = 0.0f);
 int hgrn2_status_read_and_clear(int *status);
 // HGRN2 for fp32 I/O and head dims other than 128 x 128 (CUDA cores, step by step)
+// 3-D TMA map over a row-major (d2, d1, d0) tensor with a (b0, b1, b2) box,
+// no swizzle, zero fill outside the tensor; false if the driver refuses it.
+bool encode_map_3d(CUtensorMap *tm, const void *base, CUtensorMapDataType type, size_t esize,
+                   uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2);
+
+int hgrn2_general_status_read_and_clear(int *status);
+
 int hgrn2_general_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                          void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
                          int64_t dv, int io_bf16, bool preact, float lb, cudaStream_t stream);

@@ -118,7 +118,8 @@ def general_inputs(B, L, H, dk, dv, seed, dtype):
 @pytest.mark.parametrize("dtype,tol", [(torch.float32, 1e-4), (torch.bfloat16, 1e-2)])
 @pytest.mark.parametrize("B,L,H,dk,dv", [(2, 200, 2, 128, 128), (1, 150, 3, 64, 32),
                                          (1, 97, 1, 40, 24), (1, 64, 2, 256, 128),
-                                         (1, 33, 1, 300, 16)])
+                                         (1, 33, 1, 300, 16), (1, 77, 2, 33, 7),
+                                         (1, 50, 1, 16, 200), (2, 35, 1, 512, 40)])
 def test_hgrn2_general_path_matches_oracle(lr, dtype, tol, B, L, H, dk, dv):
     if dtype == torch.bfloat16 and dk == dv == 128:
         pytest.skip("bf16 128 x 128 runs the tensor-core kernel (covered above)")
@@ -159,3 +160,25 @@ def test_hgrn2_general_path_fast_decay_has_no_range_limit(lr):
     assert lr.lr_check_status(0) == 0
     orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], 1)
     assert rel_err(o.cpu(), orf) <= 1e-4 and rel_err(Sf.cpu(), Srf) <= 1e-4
+
+
+
+@pytest.mark.parametrize("dtype,tol", [(torch.float32, 1e-4), (torch.bfloat16, 1e-2)])
+@pytest.mark.parametrize("B,L,H", [(2, 80, 64), (1, 70, 40)])
+def test_hgrn2_general_path_wide_grids(lr, dtype, tol, B, L, H):
+    """Enough heads that the general kernel gives each thread 32 key columns
+    of two value rows (2 x 64 heads) or of one row (40 heads) instead of 16
+    columns of one row."""
+    dk = dv = 128
+    if dtype == torch.bfloat16:
+        dk = dv = 64 * 2 if H == 40 else 128
+    p = general_inputs(B, L, H, dk, dv, seed=B * 7 + H, dtype=dtype)
+    if dtype == torch.bfloat16:   # 128 x 128 bf16 is the tensor-core kernel's: use chunk 32
+        o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), p["g"].cuda(), H=H, chunk=32)
+    else:
+        o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), p["g"].cuda(), H=H)
+    torch.cuda.synchronize()
+    assert lr.lr_check_status(0) == 0
+    orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], H)
+    assert rel_err(o.float().cpu(), orf) <= tol
+    assert rel_err(Sf.cpu(), Srf) <= tol
