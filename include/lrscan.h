@@ -271,6 +271,75 @@ int lr_minmax_scan_fwd(const void *r, const void *s, const float *x0, void *y,
                        void *workspace, size_t ws_bytes, lr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Host buffers                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The scans above with every tensor in HOST memory (activations, parameters,
+ * initial and final states); only the workspace is device memory, on the
+ * current device.  The pages' layers take their inputs from wherever the
+ * framework keeps them; these entry points are for callers whose data lives
+ * in host memory, so that the host <-> device traffic, which dominates such a
+ * call, overlaps the scan.
+ *
+ * The library cuts the sequence into chunks of Lc time steps (a multiple of
+ * 64, about 32 MB of inputs each) and runs each chunk with the matching
+ * device entry point, the state carried from chunk to chunk on the device;
+ * on three streams of its own it copies chunk k+1's inputs in while chunk k
+ * runs and chunk k-1's outputs go out.  Arguments, layouts, requirements and
+ * errors are those of the device call (lr_selective_scan_fwd,
+ * lr_rglru_scan_fwd, lr_hgrn2_fwd, lr_minmax_scan_fwd); results equal the
+ * device call's up to the rounding of the chunk boundaries (the same
+ * split-resume property that h0 / h_final give).
+ *
+ *   - Ownership: every host pointer stays the caller's; the call reads and
+ *     writes them until it returns, and it returns only when every output
+ *     and the final state are in host memory.  Work already queued on
+ *     `stream` completes before the library touches the workspace.
+ *   - Pinned (page-locked) host memory lets the copies run asynchronously
+ *     and overlap; pageable memory gives the same results, slower.
+ *   - workspace: at least lr_*_fwd_host_workspace_size(...) bytes of device
+ *     memory, 16-byte aligned, else LR_ERR_WORKSPACE / LR_ERR_MISALIGNED
+ *     (two chunks of inputs and of outputs, two states, the parameters and
+ *     the device call's own workspace).  The size covers the optional
+ *     tensors (z, Dskip) whether or not a call passes them.
+ *   - Calls on one device run one after another (the library's streams are
+ *     shared; a mutex serialises them).
+ */
+size_t lr_selective_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D,
+                                                 int64_t N, lr_dtype io);
+int lr_selective_scan_fwd_host(const void *x, const void *dt, const void *z,
+                               const void *Bm, const void *Cm,
+                               const float *A_log, const float *Dskip,
+                               const float *h0, void *y, float *h_final,
+                               int64_t B, int64_t L, int64_t D, int64_t N,
+                               lr_dtype io, int dt_softplus,
+                               void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+size_t lr_rglru_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D,
+                                             lr_dtype io);
+int lr_rglru_scan_fwd_host(const void *x, const void *r, const void *i,
+                           const float *a_log, float c, const float *h0,
+                           void *y, float *h_final,
+                           int64_t B, int64_t L, int64_t D, lr_dtype io,
+                           void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+size_t lr_hgrn2_fwd_host_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk,
+                                        int64_t dv, lr_dtype io);
+int lr_hgrn2_fwd_host(const void *q, const void *k, const void *v, const void *g,
+                      const float *S0, void *o, float *S_final,
+                      int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
+                      int64_t chunk, lr_dtype io,
+                      void *workspace, size_t ws_bytes, lr_stream_t stream);
+
+size_t lr_minmax_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D,
+                                              lr_dtype io);
+int lr_minmax_scan_fwd_host(const void *r, const void *s, const float *x0, void *y,
+                            float *x_final, int64_t B, int64_t L, int64_t D,
+                            lr_dtype io, void *workspace, size_t ws_bytes,
+                            lr_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Single-token decode steps                                                 */
 /* ------------------------------------------------------------------------ */
 
@@ -329,6 +398,16 @@ int lr_hgrn2_step(const void *q, const void *k, const void *v, const void *g,
  * not thread-safe.  Returns the previous value.
  */
 int lr_set_split_override(int splits);
+
+/*
+ * Tuning / test knob: the chunk length (time steps) of the host-buffer entry
+ * points (lr_*_fwd_host); 0 restores the automatic choice (a multiple of 64
+ * steps holding about 32 MB of inputs).  Any positive length is valid: chunk
+ * boundaries need not fall on a kernel tile.  Process-wide; set it before
+ * querying a host workspace size, which depends on it.  Returns the previous
+ * setting.
+ */
+int64_t lr_set_host_chunk_steps(int64_t steps);
 
 /*
  * Test hook for the bounded look-back wait: when `split` >= 1, the thread

@@ -38,6 +38,7 @@ SIGNATURES = {
     "lr_check_status": (_I, [_P]),
     "lr_set_split_override": (_I, [_I]),
     "lr_test_withhold_split": (_I, [_I, _I]),
+    "lr_set_host_chunk_steps": (_I64, [_I64]),
     "lr_selective_scan_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I]),
     "lr_selective_scan_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I64, _I64, _I64, _I64, _I, _I, _P, _SZ, _P]),
@@ -60,6 +61,17 @@ SIGNATURES = {
     "lr_rglru_scan_step": (_I, [_P, _P, _P, _P, _F, _P, _P, _P, _I64, _I64, _I, _P]),
     "lr_hgrn2_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I, _P]),
     "lr_minmax_scan_step": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I, _P]),
+    "lr_selective_scan_fwd_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I]),
+    "lr_selective_scan_fwd_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _I64, _I64, _I64, _I64, _I, _I, _P, _SZ, _P]),
+    "lr_rglru_scan_fwd_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "lr_rglru_scan_fwd_host": (_I, [_P, _P, _P, _P, _F, _P, _P, _P,
+                                    _I64, _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_hgrn2_fwd_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I]),
+    "lr_hgrn2_fwd_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                               _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_minmax_scan_fwd_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "lr_minmax_scan_fwd_host": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, _SZ, _P]),
 }
 
 
@@ -105,6 +117,11 @@ def lr_check_status(stream: int = 0) -> int:
 
 def lr_set_split_override(splits: int) -> int:
     return int(_lib.lr_set_split_override(int(splits)))
+
+
+def lr_set_host_chunk_steps(steps: int) -> int:
+    """Chunk length of the host-buffer path (0 = automatic); returns the previous."""
+    return int(_lib.lr_set_host_chunk_steps(int(steps)))
 
 
 def lr_test_withhold_split(split: int, timeout_ms: int = 1000) -> int:
@@ -191,6 +208,50 @@ def lr_hgrn2_step(q, k, v, g, S_in, S_out, o, B, H, dk, dv, io, stream) -> int:
                                   stream))
 
 
+def lr_selective_scan_fwd_host_workspace_size(B, L, D, N, io) -> int:
+    return int(_lib.lr_selective_scan_fwd_host_workspace_size(B, L, D, N, io))
+
+
+def lr_selective_scan_fwd_host(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, N, io,
+                               dt_softplus, workspace, ws_bytes, stream) -> int:
+    """Selective scan on host buffers (device workspace only)."""
+    return int(_lib.lr_selective_scan_fwd_host(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final,
+                                               B, L, D, N, io, dt_softplus, workspace, ws_bytes,
+                                               stream))
+
+
+def lr_rglru_scan_fwd_host_workspace_size(B, L, D, io) -> int:
+    return int(_lib.lr_rglru_scan_fwd_host_workspace_size(B, L, D, io))
+
+
+def lr_rglru_scan_fwd_host(x, r, i, a_log, c, h0, y, h_final, B, L, D, io, workspace, ws_bytes,
+                           stream) -> int:
+    """RG-LRU scan on host buffers (device workspace only)."""
+    return int(_lib.lr_rglru_scan_fwd_host(x, r, i, a_log, c, h0, y, h_final, B, L, D, io,
+                                           workspace, ws_bytes, stream))
+
+
+def lr_hgrn2_fwd_host_workspace_size(B, L, H, dk, dv, io) -> int:
+    return int(_lib.lr_hgrn2_fwd_host_workspace_size(B, L, H, dk, dv, io))
+
+
+def lr_hgrn2_fwd_host(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io, workspace, ws_bytes,
+                      stream) -> int:
+    """HGRN2 on host buffers (device workspace only)."""
+    return int(_lib.lr_hgrn2_fwd_host(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io,
+                                      workspace, ws_bytes, stream))
+
+
+def lr_minmax_scan_fwd_host_workspace_size(B, L, D, io) -> int:
+    return int(_lib.lr_minmax_scan_fwd_host_workspace_size(B, L, D, io))
+
+
+def lr_minmax_scan_fwd_host(r, s, x0, y, x_final, B, L, D, io, workspace, ws_bytes, stream) -> int:
+    """MinMax scan on host buffers (device workspace only)."""
+    return int(_lib.lr_minmax_scan_fwd_host(r, s, x0, y, x_final, B, L, D, io, workspace, ws_bytes,
+                                            stream))
+
+
 # ------------------------------------------------------------ torch helpers
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
@@ -271,6 +332,63 @@ def _outputs(out, specs, dev):
     return [torch.empty(sh, dtype=dt, device=dev) for sh, dt in specs], list(out)
 
 
+# ---- host buffers: the library's chunked host path (lr_*_fwd_host)
+_HOST_WS = {}
+
+
+def _host_route(acts, out) -> bool:
+    """True when every activation and every given result tensor is in host
+    memory: the call then goes to the library's host-buffer entry point."""
+    if any(t is not None and t.device.type == "cuda" for t in acts):
+        return False
+    return out is None or all(o.device.type != "cuda" for o in out)
+
+
+def _h(t: Optional[torch.Tensor], dtype=None) -> Optional[torch.Tensor]:
+    if t is None:
+        return None
+    if t.device.type == "cuda":
+        t = t.cpu()
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.contiguous()
+
+
+def _host_outputs(out, specs):
+    """Host result tensors: the caller's, or new pinned ones."""
+    if out is None:
+        return [torch.empty(sh, dtype=dt, pin_memory=True) for sh, dt in specs]
+    if len(out) != len(specs):
+        raise ValueError(f"out must hold {len(specs)} tensors")
+    for o, (sh, dt) in zip(out, specs):
+        if tuple(o.shape) != tuple(sh) or o.dtype != dt or not o.is_contiguous():
+            raise ValueError(f"out tensor {tuple(o.shape)} {o.dtype} does not match "
+                             f"{tuple(sh)} {dt} (contiguous)")
+    return list(out)
+
+
+def _host_workspace(nbytes: int, given: Optional[torch.Tensor]):
+    """Device staging for a host-buffer call: the caller's tensor, or one
+    kept per device and grown as needed."""
+    if nbytes == (1 << 64) - 1:
+        raise LrError(LR_ERR_CUDA, "workspace size query")
+    if nbytes == 0:
+        return None, 0
+    if given is not None:
+        return given, given.numel() * given.element_size()
+    dev = torch.cuda.current_device()
+    ws = _HOST_WS.get(dev)
+    if ws is None or ws.numel() < nbytes:
+        _HOST_WS.pop(dev, None)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=torch.device("cuda", dev))
+        _HOST_WS[dev] = ws
+    return ws, nbytes
+
+
+def _host_stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
 def _finish(bufs, host_out, host: bool, dev, sync_host: bool):
     if host_out is not None:
         for dst, src in zip(host_out, bufs):
@@ -289,8 +407,25 @@ def selective_scan(x, dt, Bm, Cm, A_log, z=None, Dskip=None, h0=None,
     """Selective SSM scan.  x, dt, z: (B, L, D); Bm, Cm: (B, L, 16), all one
     dtype (float32 or bfloat16); A_log: (D, 16) fp32; Dskip: (D,) fp32;
     h0: (B, D, 16) fp32.  Returns (y (B, L, D) in the I/O dtype, h_final
-    (B, D, 16) fp32).  Host inputs are copied to the GPU and results back;
-    ``out=(y, h_final)`` gives the result tensors (GPU or host)."""
+    (B, D, 16) fp32); ``out=(y, h_final)`` gives the result tensors (GPU or
+    host).  Host inputs with host (or no) ``out`` run the library's
+    host-buffer path (chunked, copies overlapping the scan; pinned memory
+    keeps the copies asynchronous); ``workspace`` is then its device
+    staging buffer."""
+    if _host_route((x, dt, z, Bm, Cm), out):
+        x, dt, z, Bm, Cm = (_h(t) for t in (x, dt, z, Bm, Cm))
+        A_log, Dskip, h0 = (_h(t, torch.float32) for t in (A_log, Dskip, h0))
+        _same(x, dt, z, Bm, Cm)
+        io = _io_of(x)
+        B, L, D = x.shape
+        N = Bm.shape[-1]
+        y, hf = _host_outputs(out, [((B, L, D), x.dtype), ((B, D, N), torch.float32)])
+        ws, wsb = _host_workspace(lr_selective_scan_fwd_host_workspace_size(B, L, D, N, io), workspace)
+        _check(lr_selective_scan_fwd_host(_ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _ptr(A_log),
+                                          _ptr(Dskip), _ptr(h0), _ptr(y), _ptr(hf), B, L, D, N, io,
+                                          int(bool(dt_softplus)), _ptr(ws), wsb, _host_stream()),
+               "lr_selective_scan_fwd_host")
+        return y, hf
     host = x.device.type != "cuda"
     dev = _target_device(x)
     x, dt, z, Bm, Cm = (_dev(t, dev) for t in (x, dt, z, Bm, Cm))
@@ -314,7 +449,21 @@ def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None, out=None
     """RG-LRU scan.  x, r, i: (B, L, D) (r, i after their sigmoid, or before
     it with ``gates_preact=True``: the kernel applies it), one dtype;
     a_log: (D,) fp32; h0: (B, D) fp32.  Returns (y (B, L, D), h_final (B, D)
-    fp32); ``out=(y, h_final)`` gives the result tensors (GPU or host)."""
+    fp32); ``out=(y, h_final)`` gives the result tensors (GPU or host).  Host
+    inputs with host (or no) ``out`` run the library's host-buffer path
+    (activated gates only)."""
+    if not gates_preact and _host_route((x, r, i), out):
+        x, r, i = (_h(t) for t in (x, r, i))
+        a_log, h0 = (_h(t, torch.float32) for t in (a_log, h0))
+        _same(x, r, i)
+        io = _io_of(x)
+        B, L, D = x.shape
+        y, hf = _host_outputs(out, [((B, L, D), x.dtype), ((B, D), torch.float32)])
+        ws, wsb = _host_workspace(lr_rglru_scan_fwd_host_workspace_size(B, L, D, io), workspace)
+        _check(lr_rglru_scan_fwd_host(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c), _ptr(h0),
+                                      _ptr(y), _ptr(hf), B, L, D, io, _ptr(ws), wsb, _host_stream()),
+               "lr_rglru_scan_fwd_host")
+        return y, hf
     host = x.device.type != "cuda"
     dev = _target_device(x)
     x, r, i = (_dev(t, dev) for t in (x, r, i))
@@ -338,10 +487,24 @@ def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None
     pre-activation f and the kernel forms lb + (1 - lb) sigmoid(f)), one
     dtype (bfloat16 or float32); S0: (B, H, dv, dk) fp32.  Returns (o (B, L, H*dv), S_final
     (B, H, dv, dk) fp32); ``out=(o, S_final)`` gives the result tensors (GPU
-    or host).  Raises ValueError when the hidden size is not divisible by
-    the head count."""
+    or host).  Host inputs with host (or no) ``out`` run the library's
+    host-buffer path (activated gates only).  Raises ValueError when the
+    hidden size is not divisible by the head count."""
     if q.shape[-1] % H or v.shape[-1] % H:
         raise ValueError(f"hidden size {q.shape[-1]} is not divisible by {H} heads")
+    if gate_lb is None and _host_route((q, k, v, g), out):
+        q, k, v, g = (_h(t) for t in (q, k, v, g))
+        S0 = _h(S0, torch.float32)
+        _same(q, k, v, g)
+        io = _io_of(q)
+        B, L, HK = q.shape
+        dk, dv = HK // H, v.shape[-1] // H
+        o, Sf = _host_outputs(out, [((B, L, H * dv), q.dtype), ((B, H, dv, dk), torch.float32)])
+        ws, wsb = _host_workspace(lr_hgrn2_fwd_host_workspace_size(B, L, H, dk, dv, io), workspace)
+        _check(lr_hgrn2_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0), _ptr(o), _ptr(Sf),
+                                 B, L, H, dk, dv, chunk, io, _ptr(ws), wsb, _host_stream()),
+               "lr_hgrn2_fwd_host")
+        return o, Sf
     host = q.device.type != "cuda"
     dev = _target_device(q)
     q, k, v, g = (_dev(t, dev) for t in (q, k, v, g))
@@ -370,7 +533,19 @@ def minmax_scan(r, s, x0=None, workspace=None, out=None,
     """MinMax recurrence x_t = max(min(r_t, x_{t-1}), s_t).  r, s: (B, L, D),
     one dtype (float32 or bfloat16); x0: (B, D) fp32 or None (zero).
     Returns (y (B, L, D) = the state after every step, x_final (B, D) fp32);
-    ``out=(y, x_final)`` gives the result tensors (GPU or host)."""
+    ``out=(y, x_final)`` gives the result tensors (GPU or host).  Host inputs
+    with host (or no) ``out`` run the library's host-buffer path."""
+    if _host_route((r, s), out):
+        r, s = (_h(t) for t in (r, s))
+        x0 = _h(x0, torch.float32)
+        _same(r, s)
+        io = _io_of(r)
+        B, L, D = r.shape
+        y, xf = _host_outputs(out, [((B, L, D), r.dtype), ((B, D), torch.float32)])
+        ws, wsb = _host_workspace(lr_minmax_scan_fwd_host_workspace_size(B, L, D, io), workspace)
+        _check(lr_minmax_scan_fwd_host(_ptr(r), _ptr(s), _ptr(x0), _ptr(y), _ptr(xf), B, L, D, io,
+                                       _ptr(ws), wsb, _host_stream()), "lr_minmax_scan_fwd_host")
+        return y, xf
     host = r.device.type != "cuda"
     dev = _target_device(r)
     r, s = (_dev(t, dev) for t in (r, s))

@@ -6,6 +6,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 
 #include "lr_internal.h"
 #include "lrscan.h"
@@ -151,6 +152,12 @@ int lr_check_status(lr_stream_t stream) {
 int lr_set_split_override(int splits) {
     const int prev = lr::g_split_override;
     lr::g_split_override = splits > 0 ? splits : 0;
+    return prev;
+}
+
+int64_t lr_set_host_chunk_steps(int64_t steps) {
+    const int64_t prev = lr::g_host_chunk_override;
+    lr::g_host_chunk_override = steps > 0 ? steps : 0;
     return prev;
 }
 
@@ -376,4 +383,284 @@ extern "C" int lr_minmax_scan_step(const void *r, const void *s, const float *x_
     }
     return lr::minmax_step_launch(r, s, x_in, x_out, y, B, D, io == LR_BF16,
                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- host buffers
+// The same scans with every tensor in host memory: the engine in lr_host.cu
+// runs the sequence through the GPU in time chunks, each chunk one call of
+// the device entry point above (so every chunk is validated and launched
+// exactly as a device call is), the state carried on the device.
+namespace {
+
+size_t io_bytes(lr_dtype io) { return io == LR_BF16 ? 2 : 4; }
+
+// the final state of an empty sequence, in host memory
+void host_state_copy(const float *s0, float *s_final, size_t count) {
+    if (s_final == nullptr || count == 0) return;
+    if (s0 != nullptr)
+        std::memcpy(s_final, s0, count * sizeof(float));
+    else
+        std::memset(s_final, 0, count * sizeof(float));
+}
+
+int host_ws_check(const lr::HostJob &j, const void *ws, size_t ws_bytes) {
+    if (j.kernel_ws == SIZE_MAX) return LR_ERR_CUDA;
+    if (ws == nullptr || ws_bytes < lr::host_workspace_bytes(j)) return LR_ERR_WORKSPACE;
+    return misaligned(ws) ? LR_ERR_MISALIGNED : LR_OK;
+}
+
+struct SelHost {
+    int64_t B, D, N;
+    lr_dtype io;
+    int dt_softplus;
+    bool has_z;
+};
+
+int sel_host_chunk(const void *c, const void *const *in, void *const *out, const void *const *par, int64_t lc,
+                   const float *s_in, float *s_out, void *kws, size_t kws_bytes, cudaStream_t st) {
+    const SelHost &a = *static_cast<const SelHost *>(c);
+    const int b = a.has_z ? 3 : 2;   // inputs: x, dt, [z], Bm, Cm
+    return lr_selective_scan_fwd(in[0], in[1], a.has_z ? in[2] : nullptr, in[b], in[b + 1],
+                                 static_cast<const float *>(par[0]), static_cast<const float *>(par[1]), s_in,
+                                 out[0], s_out, a.B, lc, a.D, a.N, a.io, a.dt_softplus, kws, kws_bytes,
+                                 reinterpret_cast<lr_stream_t>(st));
+}
+
+// The chunk length always counts z's bytes, so the workspace query (which
+// assumes z and Dskip) covers calls without them.
+lr::HostJob sel_host_job(const SelHost &a, int64_t L, const void *x, const void *dt, const void *z,
+                         const void *Bm, const void *Cm, const float *A_log, const float *Dskip,
+                         const float *h0, void *y, float *h_final, bool with_dskip) {
+    lr::HostJob j;
+    j.B = a.B;
+    j.L = L;
+    j.es = io_bytes(a.io);
+    int n = 0;
+    j.in[n++] = {x, nullptr, a.D};
+    j.in[n++] = {dt, nullptr, a.D};
+    if (a.has_z) j.in[n++] = {z, nullptr, a.D};
+    j.in[n++] = {Bm, nullptr, a.N};
+    j.in[n++] = {Cm, nullptr, a.N};
+    j.n_in = n;
+    j.out[0] = {nullptr, y, a.D};
+    j.n_out = 1;
+    j.par[0] = {A_log, size_t(a.D) * a.N * sizeof(float)};
+    j.par[1] = {Dskip, with_dskip ? size_t(a.D) * sizeof(float) : 0};
+    j.n_par = 2;
+    j.state0 = h0;
+    j.state_final = h_final;
+    j.state_bytes = size_t(a.B) * a.D * a.N * sizeof(float);
+    j.Lc = lr::host_chunk_steps(a.B, L, j.es * size_t(3 * a.D + 2 * a.N));
+    j.kernel_ws = lr_selective_scan_workspace_size(a.B, j.Lc, a.D, a.N, a.io);
+    j.launch = sel_host_chunk;
+    j.ctx = &a;
+    return j;
+}
+
+struct RgHost {
+    int64_t B, D;
+    lr_dtype io;
+    float c;
+};
+
+int rg_host_chunk(const void *c, const void *const *in, void *const *out, const void *const *par, int64_t lc,
+                  const float *s_in, float *s_out, void *kws, size_t kws_bytes, cudaStream_t st) {
+    const RgHost &a = *static_cast<const RgHost *>(c);
+    return lr_rglru_scan_fwd(in[0], in[1], in[2], static_cast<const float *>(par[0]), a.c, s_in, out[0], s_out,
+                             a.B, lc, a.D, a.io, kws, kws_bytes, reinterpret_cast<lr_stream_t>(st));
+}
+
+lr::HostJob rg_host_job(const RgHost &a, int64_t L, const void *x, const void *r, const void *i,
+                        const float *a_log, const float *h0, void *y, float *h_final) {
+    lr::HostJob j;
+    j.B = a.B;
+    j.L = L;
+    j.es = io_bytes(a.io);
+    j.in[0] = {x, nullptr, a.D};
+    j.in[1] = {r, nullptr, a.D};
+    j.in[2] = {i, nullptr, a.D};
+    j.n_in = 3;
+    j.out[0] = {nullptr, y, a.D};
+    j.n_out = 1;
+    j.par[0] = {a_log, size_t(a.D) * sizeof(float)};
+    j.n_par = 1;
+    j.state0 = h0;
+    j.state_final = h_final;
+    j.state_bytes = size_t(a.B) * a.D * sizeof(float);
+    j.Lc = lr::host_chunk_steps(a.B, L, j.es * size_t(3 * a.D));
+    j.kernel_ws = lr_rglru_scan_workspace_size(a.B, j.Lc, a.D, a.io);
+    j.launch = rg_host_chunk;
+    j.ctx = &a;
+    return j;
+}
+
+struct HgHost {
+    int64_t B, H, dk, dv, chunk;
+    lr_dtype io;
+};
+
+int hg_host_chunk(const void *c, const void *const *in, void *const *out, const void *const *, int64_t lc,
+                  const float *s_in, float *s_out, void *kws, size_t kws_bytes, cudaStream_t st) {
+    const HgHost &a = *static_cast<const HgHost *>(c);
+    return lr_hgrn2_fwd(in[0], in[1], in[2], in[3], s_in, out[0], s_out, a.B, lc, a.H, a.dk, a.dv, a.chunk, a.io,
+                        kws, kws_bytes, reinterpret_cast<lr_stream_t>(st));
+}
+
+lr::HostJob hg_host_job(const HgHost &a, int64_t L, const void *q, const void *k, const void *v,
+                        const void *g, const float *S0, void *o, float *S_final) {
+    lr::HostJob j;
+    j.B = a.B;
+    j.L = L;
+    j.es = io_bytes(a.io);
+    j.in[0] = {q, nullptr, a.H * a.dk};
+    j.in[1] = {k, nullptr, a.H * a.dk};
+    j.in[2] = {v, nullptr, a.H * a.dv};
+    j.in[3] = {g, nullptr, a.H * a.dv};
+    j.n_in = 4;
+    j.out[0] = {nullptr, o, a.H * a.dv};
+    j.n_out = 1;
+    j.n_par = 0;
+    j.state0 = S0;
+    j.state_final = S_final;
+    j.state_bytes = size_t(a.B) * a.H * a.dv * a.dk * sizeof(float);
+    j.Lc = lr::host_chunk_steps(a.B, L, j.es * size_t(2 * a.H * (a.dk + a.dv)));
+    j.kernel_ws = lr_hgrn2_workspace_size(a.B, j.Lc, a.H, a.dk, a.dv, a.io);
+    j.launch = hg_host_chunk;
+    j.ctx = &a;
+    return j;
+}
+
+struct MmHost {
+    int64_t B, D;
+    lr_dtype io;
+};
+
+int mm_host_chunk(const void *c, const void *const *in, void *const *out, const void *const *, int64_t lc,
+                  const float *s_in, float *s_out, void *kws, size_t kws_bytes, cudaStream_t st) {
+    const MmHost &a = *static_cast<const MmHost *>(c);
+    return lr_minmax_scan_fwd(in[0], in[1], s_in, out[0], s_out, a.B, lc, a.D, a.io, kws, kws_bytes,
+                              reinterpret_cast<lr_stream_t>(st));
+}
+
+lr::HostJob mm_host_job(const MmHost &a, int64_t L, const void *r, const void *s, const float *x0, void *y,
+                        float *x_final) {
+    lr::HostJob j;
+    j.B = a.B;
+    j.L = L;
+    j.es = io_bytes(a.io);
+    j.in[0] = {r, nullptr, a.D};
+    j.in[1] = {s, nullptr, a.D};
+    j.n_in = 2;
+    j.out[0] = {nullptr, y, a.D};
+    j.n_out = 1;
+    j.n_par = 0;
+    j.state0 = x0;
+    j.state_final = x_final;
+    j.state_bytes = size_t(a.B) * a.D * sizeof(float);
+    j.Lc = lr::host_chunk_steps(a.B, L, j.es * size_t(2 * a.D));
+    j.kernel_ws = lr_minmax_scan_workspace_size(a.B, j.Lc, a.D, a.io);
+    j.launch = mm_host_chunk;
+    j.ctx = &a;
+    return j;
+}
+
+}  // namespace
+
+extern "C" size_t lr_selective_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D, int64_t N,
+                                                            lr_dtype io) {
+    if (B <= 0 || L <= 0 || D <= 0 || N != 16 || !io_ok(io)) return 0;
+    const SelHost a{B, D, N, io, 1, true};
+    const lr::HostJob j = sel_host_job(a, L, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                       nullptr, nullptr, nullptr, true);
+    return j.kernel_ws == SIZE_MAX ? SIZE_MAX : lr::host_workspace_bytes(j);
+}
+
+extern "C" int lr_selective_scan_fwd_host(const void *x, const void *dt, const void *z, const void *Bm,
+                                          const void *Cm, const float *A_log, const float *Dskip,
+                                          const float *h0, void *y, float *h_final, int64_t B, int64_t L,
+                                          int64_t D, int64_t N, lr_dtype io, int dt_softplus,
+                                          void *workspace, size_t ws_bytes, lr_stream_t stream) {
+    int rc = validate_selective(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, N, io);
+    if (rc != LR_OK) return rc;
+    if (B == 0 || D == 0) return LR_OK;
+    if (L == 0) {
+        host_state_copy(h0, h_final, size_t(B) * D * N);
+        return LR_OK;
+    }
+    const SelHost a{B, D, N, io, dt_softplus, z != nullptr};
+    const lr::HostJob j = sel_host_job(a, L, x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, Dskip != nullptr);
+    if ((rc = host_ws_check(j, workspace, ws_bytes)) != LR_OK) return rc;
+    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t lr_rglru_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io) {
+    if (B <= 0 || L <= 0 || D <= 0 || !io_ok(io)) return 0;
+    const RgHost a{B, D, io, 8.0f};
+    const lr::HostJob j = rg_host_job(a, L, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+    return j.kernel_ws == SIZE_MAX ? SIZE_MAX : lr::host_workspace_bytes(j);
+}
+
+extern "C" int lr_rglru_scan_fwd_host(const void *x, const void *r, const void *i, const float *a_log, float c,
+                                      const float *h0, void *y, float *h_final, int64_t B, int64_t L,
+                                      int64_t D, lr_dtype io, void *workspace, size_t ws_bytes,
+                                      lr_stream_t stream) {
+    int rc = validate_rglru(x, r, i, a_log, c, h0, y, h_final, B, L, D, io);
+    if (rc != LR_OK) return rc;
+    if (B == 0 || D == 0) return LR_OK;
+    if (L == 0) {
+        host_state_copy(h0, h_final, size_t(B) * D);
+        return LR_OK;
+    }
+    const RgHost a{B, D, io, c};
+    const lr::HostJob j = rg_host_job(a, L, x, r, i, a_log, h0, y, h_final);
+    if ((rc = host_ws_check(j, workspace, ws_bytes)) != LR_OK) return rc;
+    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t lr_hgrn2_fwd_host_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
+                                                   lr_dtype io) {
+    if (B <= 0 || L <= 0 || H <= 0 || dk <= 0 || dv <= 0 || !io_ok(io)) return 0;
+    const HgHost a{B, H, dk, dv, 64, io};
+    const lr::HostJob j = hg_host_job(a, L, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+    return j.kernel_ws == SIZE_MAX ? SIZE_MAX : lr::host_workspace_bytes(j);
+}
+
+extern "C" int lr_hgrn2_fwd_host(const void *q, const void *k, const void *v, const void *g, const float *S0,
+                                 void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
+                                 int64_t dv, int64_t chunk, lr_dtype io, void *workspace, size_t ws_bytes,
+                                 lr_stream_t stream) {
+    int rc = validate_hgrn2(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io);
+    if (rc != LR_OK) return rc;
+    if (B == 0) return LR_OK;
+    if (L == 0) {
+        host_state_copy(S0, S_final, size_t(B) * H * dk * dv);
+        return LR_OK;
+    }
+    const HgHost a{B, H, dk, dv, chunk, io};
+    const lr::HostJob j = hg_host_job(a, L, q, k, v, g, S0, o, S_final);
+    if ((rc = host_ws_check(j, workspace, ws_bytes)) != LR_OK) return rc;
+    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t lr_minmax_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io) {
+    if (B <= 0 || L <= 0 || D <= 0 || !io_ok(io)) return 0;
+    const MmHost a{B, D, io};
+    const lr::HostJob j = mm_host_job(a, L, nullptr, nullptr, nullptr, nullptr, nullptr);
+    return j.kernel_ws == SIZE_MAX ? SIZE_MAX : lr::host_workspace_bytes(j);
+}
+
+extern "C" int lr_minmax_scan_fwd_host(const void *r, const void *s, const float *x0, void *y, float *x_final,
+                                       int64_t B, int64_t L, int64_t D, lr_dtype io, void *workspace,
+                                       size_t ws_bytes, lr_stream_t stream) {
+    int rc = validate_minmax(r, s, x0, y, x_final, B, L, D, io);
+    if (rc != LR_OK) return rc;
+    if (B == 0 || D == 0) return LR_OK;
+    if (L == 0) {
+        host_state_copy(x0, x_final, size_t(B) * D);
+        return LR_OK;
+    }
+    const MmHost a{B, D, io};
+    const lr::HostJob j = mm_host_job(a, L, r, s, x0, y, x_final);
+    if ((rc = host_ws_check(j, workspace, ws_bytes)) != LR_OK) return rc;
+    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -65,14 +65,13 @@ int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, con
                  void *o, float *S_final, int64_t B, int64_t L, int64_t H, void *workspace,
                  cudaStream_t stream, bool preact = false, float lb = 0.0f);
 int hgrn2_status_read_and_clear(int *status);
-// HGRN2 for fp32 I/O and head dims other than 128 x 128 (CUDA cores, step by step)
 // 3-D TMA map over a row-major (d2, d1, d0) tensor with a (b0, b1, b2) box,
 // no swizzle, zero fill outside the tensor; false if the driver refuses it.
 bool encode_map_3d(CUtensorMap *tm, const void *base, CUtensorMapDataType type, size_t esize,
                    uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2);
 
+// HGRN2 for fp32 I/O and head dims other than 128 x 128 (CUDA cores, step by step)
 int hgrn2_general_status_read_and_clear(int *status);
-
 int hgrn2_general_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                          void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
                          int64_t dv, int io_bf16, bool preact, float lb, cudaStream_t stream);
@@ -90,5 +89,42 @@ int minmax_step_launch(const void *r, const void *s, const float *x_in, float *x
 int hgrn2_step_launch(const void *q, const void *k, const void *v, const void *g, const float *S_in,
                       float *S_out, void *o, int64_t B, int64_t H, int64_t dk, int64_t dv, int io_bf16,
                       cudaStream_t stream);
+
+// Host-buffer runs (lr_host.cu): a scan whose tensors live in host memory is
+// moved through the GPU in chunks of Lc time steps on three streams of the
+// library's own (copy in, compute, copy out), two chunks in flight in each
+// direction, the carried state staying on the device between chunks.
+struct HostSeq {          // a (B, L, width) host array of `es`-byte elements
+    const void *in = nullptr;   // input sequence (copied in), or
+    void *out = nullptr;        // output sequence (copied out)
+    int64_t width = 0;
+};
+struct HostParam {        // a small host array copied to the device once
+    const void *host = nullptr;
+    size_t bytes = 0;
+};
+struct HostJob {
+    int64_t B = 0, L = 0, Lc = 0;
+    size_t es = 0;
+    int n_in = 0, n_out = 0, n_par = 0;
+    HostSeq in[6], out[2];
+    HostParam par[3];
+    const float *state0 = nullptr;   // host initial state (NULL: zero)
+    float *state_final = nullptr;    // host final state (NULL: not written)
+    size_t state_bytes = 0;
+    size_t kernel_ws = 0;            // device workspace of one chunk's launch
+    // one chunk: device inputs / outputs / parameters, its length, the state
+    // it starts from (NULL: zero) and ends in, the kernel workspace
+    int (*launch)(const void *ctx, const void *const *in, void *const *out, const void *const *par,
+                  int64_t lc, const float *s_in, float *s_out, void *kws, size_t kws_bytes,
+                  cudaStream_t stream) = nullptr;
+    const void *ctx = nullptr;
+};
+// chunk length: a multiple of 64 steps (every kernel's tile) holding about
+// 32 MB of inputs; `in_bytes_per_step` counts one batch row
+int64_t host_chunk_steps(int64_t B, int64_t L, size_t in_bytes_per_step);
+extern int64_t g_host_chunk_override;   // lr_set_host_chunk_steps
+size_t host_workspace_bytes(const HostJob &job);
+int run_host_job(const HostJob &job, void *workspace, size_t ws_bytes, cudaStream_t caller);
 
 }  // namespace lr
