@@ -103,6 +103,16 @@ __device__ __forceinline__ float softplus_t(float x) {
     return x > 20.0f ? x : l;
 }
 
+// Two fast-form softplus values at once (packed fp32x2 arithmetic).
+__device__ __forceinline__ float2 softplus2_fast(float2 x) {
+    const float2 t = __fmul2_rn(x, make_float2(kLog2e, kLog2e));
+    const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+    const float2 e1 = __fadd2_rn(e, make_float2(1.0f, 1.0f));
+    const float2 l = __fmul2_rn(make_float2(lg2_approx(e1.x), lg2_approx(e1.y)), make_float2(kLn2, kLn2));
+    return make_float2(x.x > 20.0f ? x.x : (e.x < 9.765625e-4f ? e.x : l.x),
+                       x.y > 20.0f ? x.y : (e.y < 9.765625e-4f ? e.y : l.y));
+}
+
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -657,14 +667,36 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
 #pragma unroll 2   // two batches in flight: the next batch's softplus overlaps this one's updates
     for (int j0 = 0; j0 < C::T; j0 += C::BATCH) {
         float xv[OWN], dl[OWN], u[OWN];
+        if (LPC == 2 && !ACC) {
+            // the lane's own steps two at a time, in packed fp32x2 arithmetic
 #pragma unroll
-        for (int m = 0; m < OWN; ++m) {
-            const int j = j0 + r + LPC * m;
-            xv[m] = Io<IO>::to_f(xs[j * DC]);
-            const float dtv = Io<IO>::to_f(dts[j * DC]);
-            dl[m] = SOFTPLUS ? softplus_t<ACC>(dtv) : dtv;
-            if (MODE != kFull) dl[m] = j < rows ? dl[m] : 0.0f;  // rows past L: identity steps
-            u[m] = dl[m] * xv[m];
+            for (int m = 0; m < OWN; m += 2) {
+                const int ja = j0 + r + LPC * m, jb = ja + LPC;
+                const float2 x2 = make_float2(Io<IO>::to_f(xs[ja * DC]), Io<IO>::to_f(xs[jb * DC]));
+                float2 d2 = make_float2(Io<IO>::to_f(dts[ja * DC]), Io<IO>::to_f(dts[jb * DC]));
+                if (SOFTPLUS) d2 = softplus2_fast(d2);
+                if (MODE != kFull) {   // rows past L: identity steps
+                    d2.x = ja < rows ? d2.x : 0.0f;
+                    d2.y = jb < rows ? d2.y : 0.0f;
+                }
+                const float2 u2 = __fmul2_rn(d2, x2);
+                xv[m] = x2.x;
+                xv[m + 1] = x2.y;
+                dl[m] = d2.x;
+                dl[m + 1] = d2.y;
+                u[m] = u2.x;
+                u[m + 1] = u2.y;
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < OWN; ++m) {
+                const int j = j0 + r + LPC * m;
+                xv[m] = Io<IO>::to_f(xs[j * DC]);
+                const float dtv = Io<IO>::to_f(dts[j * DC]);
+                dl[m] = SOFTPLUS ? softplus_t<ACC>(dtv) : dtv;
+                if (MODE != kFull) dl[m] = j < rows ? dl[m] : 0.0f;  // rows past L: identity steps
+                u[m] = dl[m] * xv[m];
+            }
         }
         float dqs[C::BATCH], uqs[C::BATCH];
         if (LPC == 2) {
@@ -730,12 +762,29 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
                     yq[q] = keep + __shfl_xor_sync(FULL, send, bb);
                 }
             }
+            if (LPC == 2 && !ACC) {
 #pragma unroll
-            for (int m = 0; m < OWN; ++m) {
-                const int j = j0 + r + LPC * m;
-                float o = fmaf(dsk, xv[m], yq[LPC * m]);
-                if (HAS_Z) o *= silu_t<ACC>(Io<IO>::to_f(zs[j * DC]));
-                if (MODE == kFull || j < rows) __stcs(yp + size_t(j) * D, Io<IO>::from_f(o));
+                for (int m = 0; m < OWN; m += 2) {
+                    const int ja = j0 + r + LPC * m, jb = ja + LPC;
+                    float2 o2 = __ffma2_rn(make_float2(dsk, dsk), make_float2(xv[m], xv[m + 1]),
+                                           make_float2(yq[LPC * m], yq[LPC * (m + 1)]));
+                    if (HAS_Z) {   // silu(z) = z/2 (1 + tanh(z/2))
+                        const float2 hz = __fmul2_rn(
+                            make_float2(Io<IO>::to_f(zs[ja * DC]), Io<IO>::to_f(zs[jb * DC])),
+                            make_float2(0.5f, 0.5f));
+                        o2 = __fmul2_rn(o2, __ffma2_rn(hz, make_float2(tanh_approx(hz.x), tanh_approx(hz.y)), hz));
+                    }
+                    if (MODE == kFull || ja < rows) __stcs(yp + size_t(ja) * D, Io<IO>::from_f(o2.x));
+                    if (MODE == kFull || jb < rows) __stcs(yp + size_t(jb) * D, Io<IO>::from_f(o2.y));
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < OWN; ++m) {
+                    const int j = j0 + r + LPC * m;
+                    float o = fmaf(dsk, xv[m], yq[LPC * m]);
+                    if (HAS_Z) o *= silu_t<ACC>(Io<IO>::to_f(zs[j * DC]));
+                    if (MODE == kFull || j < rows) __stcs(yp + size_t(j) * D, Io<IO>::from_f(o));
+                }
             }
         }
     }
