@@ -728,20 +728,33 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
 #pragma unroll
         for (int g = 0; g < C::NP / 2; ++g) {
 #pragma unroll
-            for (int q = 0; q < C::BATCH; ++q) {
-                const float *row = bc + (j0 + q) * 2 * C::N + 4 * g;
-                const float2 dd = make_float2(dqs[q], dqs[q]);
-                const float2 uu = make_float2(uqs[q], uqs[q]);
-                const float4 b4 = *reinterpret_cast<const float4 *>(row);
-                const float2 a0 = __fmul2_rn(dd, A2[2 * g]), a1 = __fmul2_rn(dd, A2[2 * g + 1]);
-                const float2 e0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
-                const float2 e1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
-                h[2 * g] = __ffma2_rn(e0, h[2 * g], __fmul2_rn(uu, make_float2(b4.x, b4.y)));
-                h[2 * g + 1] = __ffma2_rn(e1, h[2 * g + 1], __fmul2_rn(uu, make_float2(b4.z, b4.w)));
-                if (MODE != kAggregate) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(row + C::N);
-                    ya[q] = __ffma2_rn(make_float2(c4.x, c4.y), h[2 * g], ya[q]);
-                    ya[q] = __ffma2_rn(make_float2(c4.z, c4.w), h[2 * g + 1], ya[q]);
+            for (int q = 0; q < C::BATCH; q += 2) {
+                // the group's four decays at steps q and q + 1: (delta_q, delta_q+1) x (A_n, A_n)
+                const float2 dq2 = make_float2(dqs[q], dqs[q + 1]);
+                float ea[4], eb[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float an = (k & 1) ? A2[2 * g + (k >> 1)].y : A2[2 * g + (k >> 1)].x;
+                    const float2 a = __fmul2_rn(dq2, make_float2(an, an));
+                    ea[k] = ex2_approx(a.x);
+                    eb[k] = ex2_approx(a.y);
+                }
+#pragma unroll
+                for (int qq = 0; qq < 2; ++qq) {
+                    const int qi = q + qq;
+                    const float *e = qq ? eb : ea;
+                    const float *row = bc + (j0 + qi) * 2 * C::N + 4 * g;
+                    const float2 uu = make_float2(uqs[qi], uqs[qi]);
+                    const float4 b4 = *reinterpret_cast<const float4 *>(row);
+                    h[2 * g] = __ffma2_rn(make_float2(e[0], e[1]), h[2 * g],
+                                          __fmul2_rn(uu, make_float2(b4.x, b4.y)));
+                    h[2 * g + 1] = __ffma2_rn(make_float2(e[2], e[3]), h[2 * g + 1],
+                                              __fmul2_rn(uu, make_float2(b4.z, b4.w)));
+                    if (MODE != kAggregate) {
+                        const float4 c4 = *reinterpret_cast<const float4 *>(row + C::N);
+                        ya[qi] = __ffma2_rn(make_float2(c4.x, c4.y), h[2 * g], ya[qi]);
+                        ya[qi] = __ffma2_rn(make_float2(c4.z, c4.w), h[2 * g + 1], ya[qi]);
+                    }
                 }
             }
         }
