@@ -643,7 +643,9 @@ struct SelCfg {
     static constexpr size_t OFF_BAR = OFF_BC + size_t(STAGES) * T * 2 * N * 4;
     static constexpr size_t SMEM = OFF_BAR + 3 * STAGES * 8 + 16;
     static constexpr int kAgg = 1 + N, kIncl = N;
-    static_assert(T % BATCH == 0 && (DC * LPC) % 32 == 0 && (LPC == 2 || LPC == 4), "tile shape");
+    // two lanes per channel (the exchange and the packed finish assume it;
+    // four measured slower, one leaves too few warps)
+    static_assert(T % BATCH == 0 && (DC * LPC) % 32 == 0 && LPC == 2, "tile shape");
 };
 
 // One T-step tile of one lane's states.  `rows` = steps of the tile inside
@@ -663,11 +665,10 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
     using C = SelCfg<IO, DC, LPC>;
     constexpr int OWN = C::OWN;
     const unsigned FULL = 0xffffffffu;
-    const int g0 = lane & ~(LPC - 1);   // first lane of this channel's group
 #pragma unroll 2   // two batches in flight: the next batch's softplus overlaps this one's updates
     for (int j0 = 0; j0 < C::T; j0 += C::BATCH) {
         float xv[OWN], dl[OWN], u[OWN];
-        if (LPC == 2 && !ACC) {
+        if (!ACC) {
             // the lane's own steps two at a time, in packed fp32x2 arithmetic
 #pragma unroll
             for (int m = 0; m < OWN; m += 2) {
@@ -698,25 +699,17 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
                 u[m] = dl[m] * xv[m];
             }
         }
+        // the partner lane prepared the other parity of steps: one xor
+        // exchange per value, then pick own / other per step
         float dqs[C::BATCH], uqs[C::BATCH];
-        if (LPC == 2) {
-            // the partner lane prepared the other parity of steps: one xor
-            // exchange per value, then pick own / other per step
 #pragma unroll
-            for (int m = 0; m < OWN; ++m) {
-                const float od = __shfl_xor_sync(FULL, dl[m], 1);
-                const float ou = __shfl_xor_sync(FULL, u[m], 1);
-                dqs[2 * m] = r == 0 ? dl[m] : od;
-                dqs[2 * m + 1] = r == 0 ? od : dl[m];
-                uqs[2 * m] = r == 0 ? u[m] : ou;
-                uqs[2 * m + 1] = r == 0 ? ou : u[m];
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < C::BATCH; ++q) {
-                dqs[q] = __shfl_sync(FULL, dl[q / LPC], g0 | (q % LPC));
-                uqs[q] = __shfl_sync(FULL, u[q / LPC], g0 | (q % LPC));
-            }
+        for (int m = 0; m < OWN; ++m) {
+            const float od = __shfl_xor_sync(FULL, dl[m], 1);
+            const float ou = __shfl_xor_sync(FULL, u[m], 1);
+            dqs[2 * m] = r == 0 ? dl[m] : od;
+            dqs[2 * m + 1] = r == 0 ? od : dl[m];
+            uqs[2 * m] = r == 0 ? u[m] : ou;
+            uqs[2 * m + 1] = r == 0 ? ou : u[m];
         }
         if (MODE == kAggregate) {
 #pragma unroll
@@ -775,7 +768,7 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
                     yq[q] = keep + __shfl_xor_sync(FULL, send, bb);
                 }
             }
-            if (LPC == 2 && !ACC) {
+            if (!ACC) {
 #pragma unroll
                 for (int m = 0; m < OWN; m += 2) {
                     const int ja = j0 + r + LPC * m, jb = ja + LPC;

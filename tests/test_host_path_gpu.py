@@ -111,3 +111,30 @@ def test_host_path_rejects_a_small_workspace(lr, chunk):
     with pytest.raises(lr.LrError) as e:
         lr.rglru_scan(p["x"], p["r"], p["i"], p["a_log"], p["c"], workspace=ws)
     assert e.value.code == lr.LR_ERR_WORKSPACE
+
+
+def test_host_path_calls_from_two_threads_match_sequential(lr, chunk):
+    """Host-buffer calls on one device are serialised inside the library
+    (its streams and the staging workspace are shared); two Python threads
+    calling at once get the same results as one after the other."""
+    import threading
+    inputs = [pinned(wl.rglru_inputs(1, 400, 64, seed=30 + k, io="bf16", with_h0=True)) for k in range(3)]
+    ref = [lr.rglru_scan(p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"]) for p in inputs]
+    got = [None] * len(inputs)
+    errors = []
+
+    def run(k):
+        try:
+            p = inputs[k]
+            got[k] = lr.rglru_scan(p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"])
+        except Exception as e:   # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(k,)) for k in range(len(inputs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    for (y, hf), (yr, hr) in zip(got, ref):
+        assert torch.equal(y, yr) and torch.equal(hf, hr)
