@@ -130,3 +130,29 @@ def test_minmax_steps_equal_the_scan_bit_for_bit(lr, io):
     yr, xr = oracle.minmax_scan(r, s, x0)
     assert np.array_equal(torch.stack(ys, 1).double().cpu().numpy(), yr)
     assert np.array_equal(x.double().cpu().numpy(), xr)
+
+
+def test_steps_at_the_benchmark_decode_shapes(lr):
+    """One step of each form at the shapes the benchmark's decode line times
+    (RG-LRU B=8 D=2560, selective B=4 D=4096, HGRN2 B=4 H=16 d=128, bf16),
+    from a random carried state, against the oracle's one-step scan."""
+    p = wl.rglru_inputs(8, 1, 2560, seed=41, io="bf16", with_h0=True)
+    d = cuda(p)
+    y, h = lr.rglru_scan_step(d["x"][:, 0], d["r"][:, 0], d["i"][:, 0], d["a_log"], d["c"], h=d["h0"])
+    yr, hr = oracle.rglru_scan(p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"])
+    assert rel_err(y.float().cpu()[:, None], yr) <= TOL["bf16"] and rel_err(h.cpu(), hr) <= TOL["bf16"]
+
+    p = wl.selective_inputs(4, 1, 4096, seed=42, io="bf16", with_h0=True)
+    d = cuda(p)
+    y, h = lr.selective_scan_step(d["x"][:, 0], d["dt"][:, 0], d["Bm"][:, 0], d["Cm"][:, 0], d["A_log"],
+                                  z=d["z"][:, 0], Dskip=d["Dskip"], h=d["h0"])
+    yr, hr = oracle.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], p["A_log"], z=p["z"],
+                                   Dskip=p["Dskip"], h0=p["h0"])
+    assert rel_err(y.float().cpu()[:, None], yr) <= TOL["bf16"] and rel_err(h.cpu(), hr) <= TOL["bf16"]
+
+    p = wl.hgrn2_inputs(4, 1, 16, 128, seed=43, io="bf16", with_S0=True)
+    S0 = 0.1 * p["S0"]
+    o, S = lr.hgrn2_step(p["q"][:, 0].cuda(), p["k"][:, 0].cuda(), p["v"][:, 0].cuda(), p["g"][:, 0].cuda(),
+                         16, S=S0.cuda())
+    orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], 16, S0=S0)
+    assert rel_err(o.float().cpu()[:, None], orf) <= TOL["bf16"] and rel_err(S.cpu(), Srf) <= TOL["bf16"]
