@@ -90,6 +90,9 @@ def step_configs(only=None, seq_len=None):
 # readout FMA).  At 128 fp32 lanes and 32 exp2 results per clock per SM the
 # two pipes cap the update at min(128/4, 32/1) = 32 elements per clock per SM;
 # with 152 SMs at the 2070 MHz maximum clock that is 10.07 T elements/s.
+# The powers form of the decays (A_log on the multi-scale lattice) moves most
+# exp2s off the MUFU pipe but keeps four fp32 ops per element (a power-chain
+# multiply replaces the decay argument), so the same 32 per clock bound it.
 ALU_SMS = 152
 ALU_MAX_MHZ = 2070
 ALU_ELEMS_PER_CLK_SM = 32
@@ -107,7 +110,9 @@ def kernel_roofline(cfg: wl.Config, a: dict, ms: float, peaks: dict) -> dict:
         peak = alu_peak_gelem()
         return {"kernel": cfg.name, "bound": "alu", "achieved": ach, "peak": peak,
                 "unit": "Gelem/s", "frac": ach / peak, "traffic": traffic_for(cfg),
-                "peak_source": "derived: 152 SMs x 2070 MHz x 32 state updates/clk/SM"}
+                "peak_source": "derived: 152 SMs x 2070 MHz x 32 state updates/clk/SM",
+                "decay_form": "powers: the workload's A_log is on the multi-scale lattice, "
+                              "checked per warp in the kernel"}
     ach = a["bytes"] / sec / 1e9
     return {"kernel": cfg.name, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": traffic_for(cfg),
@@ -329,8 +334,9 @@ def decode_timings(lr, cfgs, dev, steps: int = 20, reps: int = 20) -> list:
 
 def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
     """Scans outside the step, timed the same way (inputs larger than L2,
-    CUDA events on the launching stream): the MinMax recurrence at the
-    RG-LRU workload's shape, bf16 I/O."""
+    CUDA events on the launching stream): the selective workload with
+    general (off-lattice) decays, the MinMax recurrence at the RG-LRU
+    workload's shape, the pre-activation gate forms and fp32 HGRN2."""
     def timed(fn):
         for _ in range(3):
             fn()
@@ -351,6 +357,21 @@ def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
                              "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}}
 
     res = []
+    # the selective workload with A_log moved off the initialisation lattice
+    # (as training moves it): the general one-exp-per-state decays
+    cfg = wl.WORKLOADS["selective_bf16"]
+    p = wl.make_inputs(cfg, device=dev)
+    gA = torch.Generator(device=dev).manual_seed(12)
+    A_off = p["A_log"] + 0.05 * torch.randn(p["A_log"].shape, device=dev, generator=gA)
+    ms = timed(lambda: lr.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], A_off, z=p["z"],
+                                         Dskip=p["Dskip"], h0=p["h0"]))
+    rl = kernel_roofline(cfg, algorithmic(cfg), ms, peaks)
+    rl["decay_form"] = "general: one exp2 per state (A_log off the lattice)"
+    rl["traffic"] = None
+    res.append({"workload": cfg.name + " A_log off the lattice", "ms": ms,
+                "tok_ch_per_s": cfg.B * cfg.L * cfg.D / (ms * 1e-3),
+                "gb_per_s": algorithmic(cfg)["bytes"] / (ms * 1e-3) / 1e9, "roofline": rl})
+    del p, A_off
     B, L, D = 8, 4096, 2560
     g = torch.Generator(device=dev).manual_seed(11)
     r = torch.randn(B, L, D, device=dev, generator=g).to(torch.bfloat16)

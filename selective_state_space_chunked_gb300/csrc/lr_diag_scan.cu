@@ -624,6 +624,17 @@ __global__ void __launch_bounds__(MmCfg<IO>::THREADS, 1)
 //   producer warp: keeps STAGES tiles of x, dt, z, B_t, C_t in flight by TMA
 //     and widens each tile's B_t, C_t rows (shared by all channels) to fp32
 //     once, so the compute lanes read them with broadcast 16-byte loads.
+// Decays.  In general each state's decay is one exp2 of delta A[n] log2(e).
+// The SSM's initialisation puts A on a lattice, A[n] = (n + 1) A[0] per
+// channel (cortexnet MultiScaleSSM.__init__: A_log[d, n] = log((n+1) 2^s)).
+// There the 16 decays of a step are the powers E, E^2, .., E^16 of
+// E = exp(delta A[0]); a lane holding states k0 .. k0+7 takes
+// (E^(k0+1), E^(k0+2)) and E^2 from three exps and the rest of its pairs as
+// P * (E^2, E^2), five exps fewer per lane and step.  The kernel checks the
+// lattice itself, per warp, from the A_log it is given: every state of every
+// channel of the warp must satisfy |A[n] - (n+1) A[0]| <= 2^-20 |A[n]| in
+// fp32, else the warp keeps the general form.  Trained A_log leaves the
+// lattice and takes the general form; nothing is assumed.
 template <typename IO, int DC_, int LPC_>
 struct SelCfg {
     static constexpr int DC = DC_;                       // channels per block
@@ -657,11 +668,12 @@ struct SelCfg {
 // and, per group, all 8 steps: the group's decays for the 8 steps are
 // independent of each other and of the state, so they issue ahead of the
 // serial h chain.
-template <typename IO, int DC, int LPC, bool ACC, bool HAS_Z, bool SOFTPLUS, int MODE>
+template <typename IO, int DC, int LPC, bool ACC, bool HAS_Z, bool SOFTPLUS, int MODE, bool LAT = false>
 __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *zs, const float *bc,
                                          const float2 (&A2)[SelCfg<IO, DC, LPC>::NP],
                                          float2 (&h)[SelCfg<IO, DC, LPC>::NP], float &dsum,
-                                         float dsk, IO *yp, int D, int rows, int r, int lane) {
+                                         float dsk, IO *yp, int D, int rows, int r, int lane,
+                                         float3 latc = make_float3(0.0f, 0.0f, 0.0f)) {
     using C = SelCfg<IO, DC, LPC>;
     constexpr int OWN = C::OWN;
     const unsigned FULL = 0xffffffffu;
@@ -718,6 +730,42 @@ __device__ __forceinline__ void sel_tile(const IO *xs, const IO *dts, const IO *
         float2 ya[C::BATCH];
 #pragma unroll
         for (int q = 0; q < C::BATCH; ++q) ya[q] = make_float2(0.0f, 0.0f);
+        if (LAT) {
+            // lattice decays: the lane's states k0 .. k0+7 decay by E^(k0+1) ..
+            // E^(k0+8), E = 2^(delta A2[0]); (E^(k0+1), E^(k0+2)) and
+            // M = E^2 from three exps, the other pairs as P * (M, M)
+#pragma unroll
+            for (int q = 0; q < C::BATCH; q += 2) {
+                const float2 dq2 = make_float2(dqs[q], dqs[q + 1]);
+                const float2 a1 = __fmul2_rn(dq2, make_float2(latc.x, latc.x));
+                const float2 a2 = __fmul2_rn(dq2, make_float2(latc.y, latc.y));
+                const float2 am = __fmul2_rn(dq2, make_float2(latc.z, latc.z));
+                const float e1[2] = {ex2_approx(a1.x), ex2_approx(a1.y)};
+                const float e2[2] = {ex2_approx(a2.x), ex2_approx(a2.y)};
+                const float em[2] = {ex2_approx(am.x), ex2_approx(am.y)};
+#pragma unroll
+                for (int qq = 0; qq < 2; ++qq) {
+                    const int qi = q + qq;
+                    const float2 mm = make_float2(em[qq], em[qq]);
+                    float2 P[C::NP];
+                    P[0] = make_float2(e1[qq], e2[qq]);
+#pragma unroll
+                    for (int k = 1; k < C::NP; ++k) P[k] = __fmul2_rn(P[k - 1], mm);
+                    const float *row = bc + (j0 + qi) * 2 * C::N;
+                    const float2 uu = make_float2(uqs[qi], uqs[qi]);
+#pragma unroll
+                    for (int g = 0; g < C::NP / 2; ++g) {
+                        const float4 b4 = *reinterpret_cast<const float4 *>(row + 4 * g);
+                        h[2 * g] = __ffma2_rn(P[2 * g], h[2 * g], __fmul2_rn(uu, make_float2(b4.x, b4.y)));
+                        h[2 * g + 1] = __ffma2_rn(P[2 * g + 1], h[2 * g + 1],
+                                                  __fmul2_rn(uu, make_float2(b4.z, b4.w)));
+                        const float4 c4 = *reinterpret_cast<const float4 *>(row + C::N + 4 * g);
+                        ya[qi] = __ffma2_rn(make_float2(c4.x, c4.y), h[2 * g], ya[qi]);
+                        ya[qi] = __ffma2_rn(make_float2(c4.z, c4.w), h[2 * g + 1], ya[qi]);
+                    }
+                }
+            }
+        } else
 #pragma unroll
         for (int g = 0; g < C::NP / 2; ++g) {
 #pragma unroll
@@ -917,6 +965,18 @@ __global__ void __launch_bounds__(SelCfg<IO, DC, LPC>::THREADS, 1)
     }
     const float dsk = (vd && Dskip != nullptr) ? Dskip[d] : 0.0f;
     float dsum = 0.0f;  // sum of delta over the aggregate pass
+    // lattice check (see above): A2[n] = (n + 1) A2[0] to 2^-20 relative for
+    // every state of every channel of the warp; channels past D pass
+    const float a20 = vd ? -expf(A_log[size_t(d) * C::N]) * kLog2e : 0.0f;
+    bool on = true;
+#pragma unroll
+    for (int q = 0; q < C::NP; ++q) {
+        const int n = r * C::NS + 2 * q;
+        on = on && fabsf(A2[q].x - float(n + 1) * a20) <= 0x1p-20f * fabsf(A2[q].x);
+        on = on && fabsf(A2[q].y - float(n + 2) * a20) <= 0x1p-20f * fabsf(A2[q].y);
+    }
+    const bool lat = __all_sync(FULL, on);
+    const float3 latc = make_float3(float(r * C::NS + 1) * a20, float(r * C::NS + 2) * a20, 2.0f * a20);
 
     for (int v = 0; v < V; ++v) {
         const int st = v % C::STAGES;
@@ -934,6 +994,9 @@ __global__ void __launch_bounds__(SelCfg<IO, DC, LPC>::THREADS, 1)
         if (agg_pass)
             sel_tile<IO, DC, LPC, ACC, HAS_Z, SOFTPLUS, kAggregate>(xs, dts, zs, bc, A2, h, dsum, dsk,
                                                                      yp, D, L - t0, r, lane);
+        else if (full_tile && lat)
+            sel_tile<IO, DC, LPC, ACC, HAS_Z, SOFTPLUS, kFull, true>(xs, dts, zs, bc, A2, h, dsum, dsk,
+                                                                      yp, D, C::T, r, lane, latc);
         else if (full_tile)
             sel_tile<IO, DC, LPC, ACC, HAS_Z, SOFTPLUS, kFull>(xs, dts, zs, bc, A2, h, dsum, dsk, yp,
                                                                 D, C::T, r, lane);

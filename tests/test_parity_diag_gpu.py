@@ -3,7 +3,10 @@
 Metric (per output, y and final state separately): max|gpu - ref| / max|ref|,
 at most 1e-4 for fp32 I/O and 1e-2 for bf16 I/O.  Oracle-sized cases span
 many tiles, ragged tails, odd channel counts and forced time splits (the
-decoupled look-back path); the full-size workloads run in the launch
+decoupled look-back path).  The selective scan has two decay forms: the
+workloads' multi-scale A_log sits on the initialisation lattice (the powers
+form), and A_log moved off it takes the general one-exp-per-state form; both
+are checked, alone and mixed in one launch.  The full-size workloads run in the launch
 configuration the benchmark times and are checked on sampled channels, which
 the oracle computes independently of one another.
 """
@@ -186,6 +189,47 @@ def test_selective_forced_time_splits_lookback(lr, splits, io):
     check_sel(lr, p, io)
 
 
+def off_lattice(A_log, seed, channels=None, scale=0.05):
+    """A_log moved off the multi-scale lattice A[n] = (n+1) A[0] (all channels,
+    or only `channels`), so the kernel's warps holding them take the general
+    one-exp-per-state decays."""
+    g = torch.Generator().manual_seed(seed)
+    noise = scale * torch.randn(A_log.shape, generator=g)
+    if channels is not None:
+        mask = torch.zeros(A_log.shape[0], 1)
+        mask[channels] = 1.0
+        noise = noise * mask
+    return (A_log + noise).float()
+
+
+@pytest.mark.parametrize("B,L,D,io", [
+    (2, 1024, 128, "f32"),
+    (2, 1000, 256, "bf16"),
+    (1, 333, 4096, "bf16"),
+])
+def test_selective_general_decays_off_lattice(lr, B, L, D, io):
+    """Trained-like A_log (off the initialisation lattice): general decays."""
+    p = wl.selective_inputs(B, L, D, seed=B + L + D + 1, io=io, with_h0=True)
+    check_sel(lr, p, io, A_log=off_lattice(p["A_log"], seed=D))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_selective_lattice_and_general_warps_in_one_launch(lr, io):
+    """Channel 5 (warp 0 of block 0) and 100 off the lattice, the rest on it:
+    both decay forms run side by side and both match the oracle."""
+    p = wl.selective_inputs(2, 640, 128, seed=41, io=io, with_h0=True)
+    check_sel(lr, p, io, A_log=off_lattice(p["A_log"], seed=5, channels=[5, 100]))
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_selective_lattice_large_steps(lr, io):
+    """Steps of delta ~ 5 (decays down to exp(-640) underflow to zero) on the
+    lattice path."""
+    p = wl.selective_inputs(2, 256, 64, seed=43, io=io, with_h0=True)
+    dt = (p["dt"].float() + 6.5).to(p["dt"].dtype)
+    check_sel(lr, p, io, dt=dt)
+
+
 def test_selective_bf16_B4_L16384_D4096_sampled_and_four_segments(lr):
     """B=4, L=16384, d_inner=4096, N=16, bf16 I/O, h0 ~ N(0,1); also run as 4
     segments of 4096 carried through the final state."""
@@ -219,6 +263,27 @@ def test_selective_bf16_B4_L16384_D4096_sampled_and_four_segments(lr):
     torch.cuda.synchronize()
     assert torch.equal(torch.cat(segs, 1), y)
     assert torch.equal(h, hf)
+
+
+def test_selective_bf16_B4_L16384_D4096_general_decays_sampled(lr):
+    """The selective workload with A_log moved off the initialisation
+    lattice: the general decays at full size, sampled channels."""
+    cfg = wl.WORKLOADS["selective_bf16"]
+    p = wl.make_inputs(cfg, device="cuda")
+    A_log = off_lattice(p["A_log"].cpu(), seed=11).cuda()
+    y, hf = lr.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], A_log, z=p["z"],
+                              Dskip=p["Dskip"], h0=p["h0"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(4)
+    b = 1
+    ds = torch.from_numpy(np.sort(np.concatenate([rng.choice(cfg.D, 20, replace=False),
+                                                  [0, cfg.D - 1]]))).cuda()
+    sub = {k: p[k][b:b + 1][:, :, ds].cpu() for k in ("x", "dt", "z")}
+    yr, hr = oracle.selective_scan(sub["x"], sub["dt"], p["Bm"][b:b + 1].cpu(),
+                                   p["Cm"][b:b + 1].cpu(), A_log[ds].cpu(), z=sub["z"],
+                                   Dskip=p["Dskip"][ds].cpu(), h0=p["h0"][b:b + 1, ds].cpu())
+    assert rel_err(y[b:b + 1][:, :, ds].float().cpu(), yr) <= TOL["bf16"]
+    assert rel_err(hf[b:b + 1, ds].cpu(), hr) <= TOL["bf16"]
 
 
 def test_selective_zero_length_returns_initial_state(lr):
