@@ -242,7 +242,7 @@ def run_oracle(kind, args, threads=0):
     return oracle.hgrn2(**args, threads=threads)
 
 
-def cpu_baseline(cfgs, repeats=1, samples=None) -> dict:
+def cpu_baseline(cfgs, repeats=1, samples=None, single_thread=False) -> dict:
     """Times the oracle on each workload's sample; the step-equivalent rate is
     total units / sum over scans of (units / sampled rate)."""
     import oracle
@@ -261,9 +261,20 @@ def cpu_baseline(cfgs, repeats=1, samples=None) -> dict:
     step_time = sum(algorithmic(c)["units"] / rates[c.name] for c in cfgs)
     desc = "; ".join(f"{c.name}: {u} of {algorithmic(c)['units']} units"
                      for c, _, _, u in samples)
-    return {"value": total_units / step_time, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "whole sequences of a channel/head subset of batch row 0 -- " + desc,
-            "per_scan_units_per_s": rates}
+    out = {"value": total_units / step_time, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": "whole sequences of a channel/head subset of batch row 0 -- " + desc,
+           "per_scan_units_per_s": rates}
+    if single_thread:
+        # the same samples on one host thread (one timed run each)
+        rates1 = {}
+        for cfg, kind, args, units in samples:
+            t0 = time.perf_counter()
+            run_oracle(kind, args, threads=1)
+            rates1[cfg.name] = units / (time.perf_counter() - t0)
+        out["single_thread"] = {
+            "value": total_units / sum(algorithmic(c)["units"] / rates1[c.name] for c in cfgs),
+            "unit": UNIT, "cores": 1, "per_scan_units_per_s": rates1}
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -514,7 +525,7 @@ def gpu_arm(args):
         line["decode"] = decode_timings(lr, cfgs, dev)
         line["extra"] = extra_timings(lr, dev, peaks)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfgs)
+        line["cpu_baseline"] = cpu_baseline(cfgs, single_thread=True)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
