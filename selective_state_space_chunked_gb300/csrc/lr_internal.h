@@ -121,7 +121,7 @@ struct HostJob {
     const void *ctx = nullptr;
 };
 // chunk length: a multiple of 64 steps (every kernel's tile) holding about
-// 32 MB of inputs; `in_bytes_per_step` counts one batch row
+// 64 MB of inputs; `in_bytes_per_step` counts one batch row
 int64_t host_chunk_steps(int64_t B, int64_t L, size_t in_bytes_per_step);
 extern int64_t g_host_chunk_override;   // lr_set_host_chunk_steps
 size_t host_workspace_bytes(const HostJob &job);
