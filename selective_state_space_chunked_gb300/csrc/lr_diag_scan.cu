@@ -253,6 +253,43 @@ __device__ __forceinline__ void rglru_tile(const IO *xs, const IO *rs, const IO 
 #pragma unroll kUnroll
     for (int j0 = 0; j0 < C::T; j0 += C::BATCH) {
         float a[C::BATCH], bb[C::BATCH];
+        if (PRE && !ACC) {
+            // two steps at a time in packed fp32x2: both gates' sigmoids (one
+            // shared reciprocal per step, as sigmoid_pair), the decays and the
+            // input terms (as rglru_ab); each lane of a packed operation rounds
+            // as the scalar one, so the results are the scalar form's bit for bit
+#pragma unroll
+            for (int u = 0; u < C::BATCH; u += 2) {
+                const int o0 = (j0 + u) * C::DC, o1 = o0 + C::DC;
+                const float2 r2 = make_float2(Io<IO>::to_f(rs[o0]), Io<IO>::to_f(rs[o1]));
+                const float2 i2 = make_float2(Io<IO>::to_f(is[o0]), Io<IO>::to_f(is[o1]));
+                const float2 x2 = make_float2(Io<IO>::to_f(xs[o0]), Io<IO>::to_f(xs[o1]));
+                const float2 tr = __fmul2_rn(r2, make_float2(-kLog2e, -kLog2e));
+                const float2 ti = __fmul2_rn(i2, make_float2(-kLog2e, -kLog2e));
+                const float2 er1 = __fadd2_rn(make_float2(fminf(ex2_approx(tr.x), 0x1p60f),
+                                                          fminf(ex2_approx(tr.y), 0x1p60f)),
+                                              make_float2(1.0f, 1.0f));
+                const float2 ei1 = __fadd2_rn(make_float2(fminf(ex2_approx(ti.x), 0x1p60f),
+                                                          fminf(ex2_approx(ti.y), 0x1p60f)),
+                                              make_float2(1.0f, 1.0f));
+                const float2 den = __fmul2_rn(er1, ei1);
+                const float2 inv = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+                const float2 sr = __fmul2_rn(ei1, inv), si = __fmul2_rn(er1, inv);
+                const float2 la = __fmul2_rn(sr, make_float2(cl2, cl2));
+                const float2 a2 = make_float2(ex2_approx(la.x), ex2_approx(la.y));
+                const float2 om = __ffma2_rn(make_float2(-a2.x, -a2.y), a2, make_float2(1.0f, 1.0f));
+                const float2 u2 = __fmul2_rn(si, x2);
+                const float2 b2 = __fmul2_rn(make_float2(sqrt_approx(om.x), sqrt_approx(om.y)), u2);
+                a[u] = a2.x;
+                a[u + 1] = a2.y;
+                bb[u] = b2.x;
+                bb[u + 1] = b2.y;
+                if (MODE != kFull) {   // rows past L: identity steps
+                    if (j0 + u >= rows) { a[u] = 1.0f; bb[u] = 0.0f; }
+                    if (j0 + u + 1 >= rows) { a[u + 1] = 1.0f; bb[u + 1] = 0.0f; }
+                }
+            }
+        } else
 #pragma unroll
         for (int u = 0; u < C::BATCH; ++u) {
             const int o = (j0 + u) * C::DC;
