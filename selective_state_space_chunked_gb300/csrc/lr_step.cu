@@ -22,48 +22,59 @@ constexpr int kStepThreads = 128;
 
 __device__ __forceinline__ float softplus_acc(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
 
-// Selective SSM, one thread per (b, d) with its 16 states:
+// Selective SSM, four lanes per (b, d), four of its 16 states each (so the
+// state moves in coalesced 16-byte pieces and each lane runs a quarter of
+// the exp chain):
 //   delta = softplus(dt); h[n] = exp(delta A[n]) h[n] + delta B[n] x;
 //   y = (sum_n C[n] h[n] + D x) silu(z)
+// Every lane computes delta and u itself (cheap, shared loads); the partial
+// C . h sums meet by two xor shuffles and the group's first lane stores y.
+// A lane reads its 16 bytes of h_in before writing the same 16 bytes of
+// h_out, so the update may run in place.
 template <typename IO, bool HAS_Z, bool SOFTPLUS>
 __global__ void __launch_bounds__(kStepThreads)
     selective_step_kernel(const IO *__restrict__ x, const IO *__restrict__ dt, const IO *__restrict__ z,
                           const IO *__restrict__ Bm, const IO *__restrict__ Cm,
                           const float *__restrict__ A_log, const float *__restrict__ Dskip,
                           const float *h_in, float *h_out, IO *__restrict__ y, int64_t B, int64_t D) {
-    const int64_t idx = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
-    if (idx >= B * D) return;
-    const int64_t b = idx / D, d = idx - b * D;
-    const float xv = Io<IO>::to_f(x[idx]);
-    const float dtv = Io<IO>::to_f(dt[idx]);
-    const float dl = SOFTPLUS ? softplus_acc(dtv) : dtv;
-    const float u = dl * xv;
-    const IO *Bb = Bm + b * 16, *Cb = Cm + b * 16;
-    const float4 *al = reinterpret_cast<const float4 *>(A_log + d * 16);
-    const float4 *hi = h_in != nullptr ? reinterpret_cast<const float4 *>(h_in + idx * 16) : nullptr;
-    float4 *ho = reinterpret_cast<float4 *>(h_out + idx * 16);
-    float acc = 0.0f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        float4 h = hi != nullptr ? hi[q] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        const float4 a4 = al[q];
+    const int64_t g = int64_t(blockIdx.x) * kStepThreads + threadIdx.x;
+    const int64_t idx = g >> 2;            // (b, d)
+    const int q = int(g & 3);              // states 4q .. 4q+3
+    const bool valid = idx < B * D;        // whole groups of four share validity
+    float acc = 0.0f, xv = 0.0f;
+    int64_t d = 0;
+    if (valid) {
+        const int64_t b = idx / D;
+        d = idx - b * D;
+        xv = Io<IO>::to_f(x[idx]);
+        const float dtv = Io<IO>::to_f(dt[idx]);
+        const float dl = SOFTPLUS ? softplus_acc(dtv) : dtv;
+        const float u = dl * xv;
+        const IO *Bb = Bm + b * 16 + 4 * q, *Cb = Cm + b * 16 + 4 * q;
+        const float4 a4 = reinterpret_cast<const float4 *>(A_log + d * 16)[q];
+        float4 h = h_in != nullptr ? reinterpret_cast<const float4 *>(h_in + idx * 16)[q]
+                                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         float *hv = reinterpret_cast<float *>(&h);
         const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int n = 4 * q + e;
             const float decay = expf(dl * -expf(av[e]));
-            hv[e] = fmaf(decay, hv[e], u * Io<IO>::to_f(Bb[n]));
-            acc = fmaf(Io<IO>::to_f(Cb[n]), hv[e], acc);
+            hv[e] = fmaf(decay, hv[e], u * Io<IO>::to_f(Bb[e]));
+            acc = fmaf(Io<IO>::to_f(Cb[e]), hv[e], acc);
         }
-        ho[q] = h;
+        reinterpret_cast<float4 *>(h_out + idx * 16)[q] = h;
     }
-    float o = fmaf(Dskip != nullptr ? Dskip[d] : 0.0f, xv, acc);
-    if (HAS_Z) {
-        const float zv = Io<IO>::to_f(z[idx]);
-        o *= zv / (1.0f + expf(-zv));
+    // the four lanes of a group are consecutive lanes of one warp
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    if (valid && q == 0) {
+        float o = fmaf(Dskip != nullptr ? Dskip[d] : 0.0f, xv, acc);
+        if (HAS_Z) {
+            const float zv = Io<IO>::to_f(z[idx]);
+            o *= zv / (1.0f + expf(-zv));
+        }
+        y[idx] = Io<IO>::from_f(o);
     }
-    y[idx] = Io<IO>::from_f(o);
 }
 
 // RG-LRU, one thread per (b, d):
@@ -156,7 +167,7 @@ template <typename IO>
 int selective_step_io(const void *x, const void *dt, const void *z, const void *Bm, const void *Cm,
                       const float *A_log, const float *Dskip, const float *h_in, float *h_out, void *y,
                       int64_t B, int64_t D, int dt_softplus, cudaStream_t s) {
-    const unsigned grid = blocks_for(B * D, kStepThreads);
+    const unsigned grid = blocks_for(4 * B * D, kStepThreads);   // four lanes per (b, d)
     const IO *xi = static_cast<const IO *>(x), *di = static_cast<const IO *>(dt),
              *zi = static_cast<const IO *>(z), *bi = static_cast<const IO *>(Bm),
              *ci = static_cast<const IO *>(Cm);
