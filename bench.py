@@ -343,6 +343,14 @@ def decode_timings(lr, cfgs, dev, steps: int = 20, reps: int = 20) -> list:
     return res
 
 
+def off_lattice_A_log(A_log: torch.Tensor) -> torch.Tensor:
+    """A_log moved off the multi-scale initialisation lattice (seeded noise of
+    0.05), as training moves it: the selective kernel then takes its general
+    one-exp-per-state decays."""
+    g = torch.Generator(device=A_log.device).manual_seed(12)
+    return A_log + 0.05 * torch.randn(A_log.shape, device=A_log.device, generator=g)
+
+
 def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
     """Scans outside the step, timed the same way (inputs larger than L2,
     CUDA events on the launching stream): the selective workload with
@@ -372,8 +380,7 @@ def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
     # (as training moves it): the general one-exp-per-state decays
     cfg = wl.WORKLOADS["selective_bf16"]
     p = wl.make_inputs(cfg, device=dev)
-    gA = torch.Generator(device=dev).manual_seed(12)
-    A_off = p["A_log"] + 0.05 * torch.randn(p["A_log"].shape, device=dev, generator=gA)
+    A_off = off_lattice_A_log(p["A_log"])
     ms = timed(lambda: lr.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], A_off, z=p["z"],
                                          Dskip=p["Dskip"], h0=p["h0"]))
     rl = kernel_roofline(cfg, algorithmic(cfg), ms, peaks)
@@ -425,6 +432,10 @@ def gpu_arm(args):
     from selective_state_space_chunked_gb300 import binding as lr
     cfgs = step_configs(args.only, args.seq_len)
     inputs = [wl.make_inputs(c, device=dev) for c in cfgs]
+    if args.a_log_off_lattice:
+        for c, p in zip(cfgs, inputs):
+            if c.form == "selective":
+                p["A_log"] = off_lattice_A_log(p["A_log"])
     calls = [make_call(lr, c, p) for c, p in zip(cfgs, inputs)]
     alg = [algorithmic(c) for c in cfgs]
     stream = torch.cuda.current_stream(dev)
@@ -499,6 +510,11 @@ def gpu_arm(args):
     peaks = load_peaks()
     dom = max(range(len(cfgs)), key=lambda j: per_scan[j]["ms"])
     rooflines = [kernel_roofline(c, a, d["ms"], peaks) for c, a, d in zip(cfgs, alg, per_scan)]
+    if args.a_log_off_lattice:
+        for r in rooflines:
+            if "decay_form" in r:
+                r["decay_form"] = "general: one exp2 per state (A_log off the lattice)"
+                r["traffic"] = None
     roof = dict(rooflines[dom])
     for d in per_scan:
         d["hbm_frac"] = d["gb_per_s"] / peaks["hbm_gbs"]
@@ -521,6 +537,8 @@ def gpu_arm(args):
         "gpu_launches": len(cfgs) * args.steps,
         "clocks": clk,
     }
+    if args.a_log_off_lattice:
+        line["config"]["selective_A_log"] = "moved off the initialisation lattice (profiling case)"
     if not args.seq_len and not args.only and not args.no_extras:
         line["decode"] = decode_timings(lr, cfgs, dev)
         line["extra"] = extra_timings(lr, dev, peaks)
@@ -625,6 +643,9 @@ def main():
                     help="run one scan of the step (profiling case)")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="shorter sequences for a profiling case (not a benchmark number)")
+    ap.add_argument("--a-log-off-lattice", action="store_true",
+                    help="selective A_log moved off the initialisation lattice (the general "
+                         "decay form; a profiling case, not the workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
