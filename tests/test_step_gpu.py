@@ -72,6 +72,21 @@ def test_hgrn2_step_matches_oracle(lr, io, dk, dv, H):
     assert rel_err(S.cpu(), Srf) <= TOL[io]
 
 
+@pytest.mark.parametrize("B,D", [(1, 8), (3, 40)])
+def test_selective_step_partial_last_block(lr, B, D):
+    """Four lanes per channel: 4*B*D threads that do not fill the last
+    128-thread block (the idle lanes still join the readout shuffles), and
+    the zero initial state."""
+    p = wl.selective_inputs(B, 1, D, seed=36 + D, io="f32", with_h0=False)
+    d = cuda(p)
+    y, h = lr.selective_scan_step(d["x"][:, 0], d["dt"][:, 0], d["Bm"][:, 0], d["Cm"][:, 0],
+                                  d["A_log"], z=d["z"][:, 0], Dskip=d["Dskip"], h=None)
+    yr, hr = oracle.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], p["A_log"], z=p["z"],
+                                   Dskip=p["Dskip"])
+    assert rel_err(y.float().cpu()[:, None], yr) <= TOL["f32"]
+    assert rel_err(h.cpu(), hr) <= TOL["f32"]
+
+
 def test_chained_steps_follow_the_sequence_in_place(lr):
     """20 steps with the state updated in place equal the oracle over L = 20."""
     L = 20
