@@ -280,14 +280,38 @@ def cpu_baseline(cfgs, repeats=1, samples=None, single_thread=False) -> dict:
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
-def make_call(lr, cfg, p, out=None):
+def make_call(lr, cfg, p, out=None, ws=None):
+    """One call of a workload's scan through the public torch API; ``ws``: the
+    workspace tensor it keeps using (its first bytes hold each call's device
+    status)."""
     if cfg.form == "rglru":
         return lambda: lr.rglru_scan(p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"],
-                                     out=out)
+                                     out=out, workspace=ws)
     if cfg.form == "selective":
         return lambda: lr.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], p["A_log"],
-                                         z=p["z"], Dskip=p["Dskip"], h0=p["h0"], out=out)
-    return lambda: lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=p["H"], out=out)
+                                         z=p["z"], Dskip=p["Dskip"], h0=p["h0"], out=out,
+                                         workspace=ws)
+    return lambda: lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=p["H"], out=out, workspace=ws)
+
+
+def workspace_for(lr, cfg, dev):
+    """The device workspace of one workload's device call."""
+    io = lr.LR_BF16 if cfg.io == "bf16" else lr.LR_F32
+    if cfg.form == "rglru":
+        n = lr.lr_rglru_scan_workspace_size(cfg.B, cfg.L, cfg.D, io)
+    elif cfg.form == "selective":
+        n = lr.lr_selective_scan_workspace_size(cfg.B, cfg.L, cfg.D, cfg.N, io)
+    else:
+        n = lr.lr_hgrn2_workspace_size(cfg.B, cfg.L, cfg.H, cfg.head_dim, cfg.head_dim, io)
+    return torch.empty(max(int(n), 256), dtype=torch.uint8, device=dev)
+
+
+def check_calls(lr, wss, stream, when):
+    """Raises if any workload's latest call recorded a device-side error."""
+    for ws in wss:
+        code = lr.status(ws, stream)
+        if code != 0:
+            raise RuntimeError(f"device status {lr.lr_status_string(code)} {when}")
 
 
 def decode_timings(lr, cfgs, dev, steps: int = 20, reps: int = 20) -> list:
@@ -436,7 +460,8 @@ def gpu_arm(args):
         for c, p in zip(cfgs, inputs):
             if c.form == "selective":
                 p["A_log"] = off_lattice_A_log(p["A_log"])
-    calls = [make_call(lr, c, p) for c, p in zip(cfgs, inputs)]
+    wss = [workspace_for(lr, c, dev) for c in cfgs]
+    calls = [make_call(lr, c, p, ws=w) for c, p, w in zip(cfgs, inputs, wss)]
     alg = [algorithmic(c) for c in cfgs]
     stream = torch.cuda.current_stream(dev)
 
@@ -444,8 +469,7 @@ def gpu_arm(args):
         for fn in calls:
             fn()
     torch.cuda.synchronize()
-    if lr.lr_check_status(stream.cuda_stream) != 0:
-        raise RuntimeError("device status error during warm-up")
+    check_calls(lr, wss, stream, "during warm-up")
 
     clocks = ClockSampler(local)
     if rank == 0:
@@ -467,9 +491,7 @@ def gpu_arm(args):
     clk = clocks.stop() if rank == 0 else None
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, world, dev)
-    status = lr.lr_check_status(stream.cuda_stream)
-    if status != 0:
-        raise RuntimeError(f"device status {lr.lr_status_string(status)}")
+    check_calls(lr, wss, stream, "in the timed region")
 
     per_scan = []
     for j, c in enumerate(cfgs):

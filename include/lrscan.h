@@ -78,10 +78,21 @@ const char *lr_status_string(int code);
 int lr_version(void);
 
 /*
- * Synchronises `stream`, then returns and clears the device-side sticky
- * status of the current device (LR_OK when no kernel reported an error).
+ * Device-side status of the latest call that used `workspace`.
+ *
+ * Every call that takes a workspace keeps its device-side status in the
+ * workspace's first 256 bytes: each call stamps them afresh, so they describe
+ * that call alone, whatever the memory held before (no initialisation is
+ * needed).  lr_check_status synchronises `stream` -- the stream the call was
+ * made on -- then returns the status recorded there (LR_OK, or e.g.
+ * LR_ERR_TIMEOUT when a bounded wait of that call ran out; the call's
+ * outputs are then not meaningful) and resets it to LR_OK.  Concurrent calls
+ * on different streams with distinct workspaces are checked independently.
+ * workspace == NULL reads the status of the latest
+ * lr_rglru_scan_fwd_noalloc call on the current device (kept in that entry
+ * point's built-in scratch).  Returns LR_ERR_CUDA if a CUDA call fails.
  */
-int lr_check_status(lr_stream_t stream);
+int lr_check_status(void *workspace, lr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Selective SSM scan                                                        */

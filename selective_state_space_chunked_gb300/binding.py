@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional, Tuple
 
 import torch
@@ -35,7 +36,7 @@ _P, _I64, _F, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.
 SIGNATURES = {
     "lr_status_string": (ctypes.c_char_p, [_I]),
     "lr_version": (_I, []),
-    "lr_check_status": (_I, [_P]),
+    "lr_check_status": (_I, [_P, _P]),
     "lr_set_split_override": (_I, [_I]),
     "lr_test_withhold_split": (_I, [_I, _I]),
     "lr_set_host_chunk_steps": (_I64, [_I64]),
@@ -111,8 +112,11 @@ def lr_version() -> int:
     return int(_lib.lr_version())
 
 
-def lr_check_status(stream: int = 0) -> int:
-    return int(_lib.lr_check_status(stream or None))
+def lr_check_status(workspace, stream: int = 0) -> int:
+    """Status of the latest call that used ``workspace`` (a device pointer;
+    None = the built-in scratch of lr_rglru_scan_fwd_noalloc); synchronises
+    ``stream`` and resets the status."""
+    return int(_lib.lr_check_status(workspace or None, stream or None))
 
 
 def lr_set_split_override(splits: int) -> int:
@@ -267,6 +271,7 @@ def _dev(t: Optional[torch.Tensor], device) -> Optional[torch.Tensor]:
 
 def _check(rc: int, where: str):
     if rc != LR_OK:
+        _tls.ws = None   # a call that failed on the host recorded no device status
         raise LrError(rc, where)
 
 
@@ -282,14 +287,28 @@ def _same(ref: torch.Tensor, *ts):
             raise TypeError("all activation tensors must share one dtype")
 
 
+# The workspace of this thread's latest call through the torch helpers: its
+# first bytes hold that call's device-side status (see status()).
+_tls = threading.local()
+
+
+def last_workspace() -> Optional[torch.Tensor]:
+    """Workspace tensor of this thread's latest call through a torch helper."""
+    return getattr(_tls, "ws", None)
+
+
 def _workspace(nbytes: int, device, given: Optional[torch.Tensor]):
     if nbytes == (1 << 64) - 1:
         raise LrError(LR_ERR_CUDA, "workspace size query")
     if nbytes == 0:
+        _tls.ws = None
         return None, 0
     if given is not None:
-        return given, given.numel() * given.element_size()
-    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+        ws, n = given, given.numel() * given.element_size()
+    else:
+        ws, n = torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+    _tls.ws = ws
+    return ws, n
 
 
 def _target_device(*ts):
@@ -375,6 +394,7 @@ def _host_workspace(nbytes: int, given: Optional[torch.Tensor]):
     if nbytes == 0:
         return None, 0
     if given is not None:
+        _tls.ws = given
         return given, given.numel() * given.element_size()
     dev = torch.cuda.current_device()
     ws = _HOST_WS.get(dev)
@@ -382,6 +402,7 @@ def _host_workspace(nbytes: int, given: Optional[torch.Tensor]):
         _HOST_WS.pop(dev, None)
         ws = torch.empty(nbytes, dtype=torch.uint8, device=torch.device("cuda", dev))
         _HOST_WS[dev] = ws
+    _tls.ws = ws
     return ws, nbytes
 
 
@@ -643,7 +664,18 @@ def hgrn2_step(q, k, v, g, H: int, S=None, S_out=None):
     return o, S_new
 
 
-def check_status(stream=None) -> None:
-    """Synchronises the stream and raises on a device-side status."""
-    s = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
-    _check(lr_check_status(s), "device status")
+def status(workspace=None, stream=None) -> int:
+    """Device-side status code of the latest call that used ``workspace`` (a
+    tensor; default: the workspace of this thread's latest call through the
+    torch helpers); synchronises the stream (default: current) and resets
+    the status to LR_OK."""
+    ws = workspace if workspace is not None else last_workspace()
+    if ws is None:
+        return LR_OK
+    s = (stream if stream is not None else torch.cuda.current_stream(ws.device)).cuda_stream
+    return lr_check_status(ws.data_ptr(), s)
+
+
+def check_status(workspace=None, stream=None) -> None:
+    """As :func:`status`, raising :class:`LrError` on a non-zero code."""
+    _check(status(workspace, stream), "device status")

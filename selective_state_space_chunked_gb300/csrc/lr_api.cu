@@ -1,8 +1,9 @@
 // lr_api.cu -- the C ABI declared in include/lrscan.h: argument validation
 // (pure host logic, run before any CUDA call), dispatch to the kernels'
-// launchers, the sticky device status, and the tuning / test knobs.
+// launchers, the per-call device status, and the tuning / test knobs.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -15,6 +16,50 @@ namespace lr {
 int g_split_override = 0;
 int g_withheld_split = -1;
 int g_withheld_timeout_ms = 1000;
+
+namespace {
+std::atomic<unsigned long long> g_stamp{0};
+thread_local unsigned long long t_shared_stamp = 0;
+thread_local int t_shared_depth = 0;
+
+unsigned long long fresh_stamp() {
+    unsigned long long s = 0;
+    while (s == 0) s = (g_stamp.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 48) - 1);
+    return s;
+}
+}  // namespace
+
+StatusRef call_status(void *workspace) {
+    return StatusRef{static_cast<unsigned long long *>(workspace),
+                     t_shared_depth > 0 ? t_shared_stamp : fresh_stamp()};
+}
+
+SharedStamp::SharedStamp() {
+    if (t_shared_depth++ == 0) t_shared_stamp = fresh_stamp();
+}
+SharedStamp::~SharedStamp() { --t_shared_depth; }
+
+int read_status(void *workspace, cudaStream_t stream, int *code, bool clear) {
+    unsigned long long word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return LR_ERR_CUDA;
+    *code = static_cast<int>(static_cast<int16_t>(word & 0xffffu));
+    if (clear && *code != LR_OK) {
+        static const unsigned long long kZero = 0;
+        // stamp 0 with code 0: no call's stamp, nothing recorded
+        if (cudaMemcpyAsync(workspace, &kZero, sizeof(kZero), cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess)
+            return LR_ERR_CUDA;
+    }
+    return LR_OK;
+}
+
+int status_ok_no_launch(void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (workspace == nullptr || ws_bytes < kStatusBytes) return LR_OK;
+    return cudaMemsetAsync(workspace, 0, sizeof(unsigned long long), stream) == cudaSuccess ? LR_OK
+                                                                                              : LR_ERR_CUDA;
+}
 }  // namespace lr
 
 namespace {
@@ -139,14 +184,15 @@ const char *lr_status_string(int code) {
 
 int lr_version(void) { return kVersion; }
 
-int lr_check_status(lr_stream_t stream) {
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return LR_ERR_CUDA;
-    int s1 = 0, s2 = 0, s3 = 0;
-    if (lr::diag_status_read_and_clear(&s1) != LR_OK) return LR_ERR_CUDA;
-    if (lr::hgrn2_status_read_and_clear(&s2) != LR_OK) return LR_ERR_CUDA;
-    if (lr::hgrn2_general_status_read_and_clear(&s3) != LR_OK) return LR_ERR_CUDA;
-    return s1 != 0 ? s1 : (s2 != 0 ? s2 : s3);
+int lr_check_status(void *workspace, lr_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LR_ERR_CUDA;
+    void *ws = workspace;
+    if (ws == nullptr && lr::rglru_builtin_scratch(&ws) != LR_OK) return LR_ERR_CUDA;
+    if (misaligned(ws)) return LR_ERR_MISALIGNED;
+    int code = LR_OK;
+    if (lr::read_status(ws, st, &code, true) != LR_OK) return LR_ERR_CUDA;
+    return code;
 }
 
 int lr_set_split_override(int splits) {
@@ -169,7 +215,8 @@ int lr_test_withhold_split(int split, int timeout_ms) {
 
 // ---------------------------------------------------------------- selective
 size_t lr_selective_scan_workspace_size(int64_t B, int64_t L, int64_t D, int64_t N, lr_dtype io) {
-    if (B <= 0 || L <= 0 || D <= 0 || N != 16 || !io_ok(io)) return 0;
+    if (B < 0 || L < 0 || D < 0 || N != 16 || !io_ok(io)) return 0;
+    if (B == 0 || L == 0 || D == 0) return lr::kStatusBytes;
     lr::DiagPlan p;
     if (lr::selective_plan(B, L, D, io, &p) != LR_OK) return SIZE_MAX;
     return p.ws_bytes;
@@ -183,8 +230,11 @@ int lr_selective_scan_fwd(const void *x, const void *dt, const void *z, const vo
     int rc = validate_selective(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, N, io);
     if (rc != LR_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (B == 0 || D == 0) return LR_OK;
-    if (L == 0) return copy_state(h0, h_final, size_t(B) * D * N, st);
+    if (B == 0 || D == 0) return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    if (L == 0) {
+        if ((rc = copy_state(h0, h_final, size_t(B) * D * N, st)) != LR_OK) return rc;
+        return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    }
     lr::DiagPlan p;
     if ((rc = lr::selective_plan(B, L, D, io, &p)) != LR_OK) return rc;
     if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
@@ -194,7 +244,8 @@ int lr_selective_scan_fwd(const void *x, const void *dt, const void *z, const vo
 
 // ---------------------------------------------------------------- RG-LRU
 size_t lr_rglru_scan_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io) {
-    if (B <= 0 || L <= 0 || D <= 0 || !io_ok(io)) return 0;
+    if (B < 0 || L < 0 || D < 0 || !io_ok(io)) return 0;
+    if (B == 0 || L == 0 || D == 0) return lr::kStatusBytes;
     lr::DiagPlan p;
     if (lr::rglru_plan(B, L, D, io, &p) != LR_OK) return SIZE_MAX;
     return p.ws_bytes;
@@ -206,8 +257,11 @@ int lr_rglru_scan_fwd(const void *x, const void *r, const void *i, const float *
     int rc = validate_rglru(x, r, i, a_log, c, h0, y, h_final, B, L, D, io);
     if (rc != LR_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (B == 0 || D == 0) return LR_OK;
-    if (L == 0) return copy_state(h0, h_final, size_t(B) * D, st);
+    if (B == 0 || D == 0) return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    if (L == 0) {
+        if ((rc = copy_state(h0, h_final, size_t(B) * D, st)) != LR_OK) return rc;
+        return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    }
     lr::DiagPlan p;
     if ((rc = lr::rglru_plan(B, L, D, io, &p)) != LR_OK) return rc;
     if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
@@ -223,13 +277,16 @@ int lr_rglru_scan_fwd_noalloc(const void *x, const void *r, const void *i, const
     int rc = validate_rglru(x, r, i, a_log, c, h0, y, h_final, B, L, D, io);
     if (rc != LR_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (B == 0 || D == 0) return LR_OK;
-    if (L == 0) return copy_state(h0, h_final, size_t(B) * D, st);
+    void *scratch = nullptr;
+    if ((rc = lr::rglru_builtin_scratch(&scratch)) != LR_OK) return rc;
+    if (B == 0 || D == 0) return lr::status_ok_no_launch(scratch, lr::kRglruScratchBytes, st);
+    if (L == 0) {
+        if ((rc = copy_state(h0, h_final, size_t(B) * D, st)) != LR_OK) return rc;
+        return lr::status_ok_no_launch(scratch, lr::kRglruScratchBytes, st);
+    }
     lr::DiagPlan p;
     if ((rc = lr::rglru_plan(B, L, D, io, &p)) != LR_OK) return rc;
     if (p.ws_bytes > lr::kRglruScratchBytes) return LR_ERR_WORKSPACE;
-    void *scratch = nullptr;
-    if (p.ws_bytes > 0 && (rc = lr::rglru_builtin_scratch(&scratch)) != LR_OK) return rc;
     return lr::rglru_launch(x, r, i, a_log, c, h0, y, h_final, B, L, D, io, p, scratch, st);
 }
 
@@ -240,7 +297,7 @@ size_t lr_hgrn2_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk, int6
     (void)dv;
     (void)io;
     size_t bytes = 0;
-    if (B <= 0 || L <= 0 || H <= 0) return 0;
+    if (B < 0 || L < 0 || H <= 0) return 0;
     if (lr::hgrn2_workspace(B, L, H, &bytes) != LR_OK) return SIZE_MAX;
     return bytes;
 }
@@ -252,15 +309,18 @@ int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g, con
     int rc = validate_hgrn2(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io);
     if (rc != LR_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (B == 0) return LR_OK;
-    if (L == 0) return copy_state(S0, S_final, size_t(B) * H * dk * dv, st);
+    if (B == 0) return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    if (L == 0) {
+        if ((rc = copy_state(S0, S_final, size_t(B) * H * dk * dv, st)) != LR_OK) return rc;
+        return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    }
     size_t need = 0;
     if ((rc = lr::hgrn2_workspace(B, L, H, &need)) != LR_OK) return rc;
-    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return LR_ERR_WORKSPACE;
+    if (workspace == nullptr || ws_bytes < need) return LR_ERR_WORKSPACE;
     if (misaligned(workspace)) return LR_ERR_MISALIGNED;
     if (!hgrn2_tensor_path(dk, dv, chunk, io))
         return lr::hgrn2_general_launch(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, io == LR_BF16,
-                                        false, 0.0f, st);
+                                        false, 0.0f, workspace, st);
     return lr::hgrn2_launch(q, k, v, g, S0, o, S_final, B, L, H, workspace, st);
 }
 
@@ -311,7 +371,8 @@ extern "C" int lr_hgrn2_step(const void *q, const void *k, const void *v, const 
 }
 
 extern "C" size_t lr_minmax_scan_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io) {
-    if (B <= 0 || L <= 0 || D <= 0 || !io_ok(io)) return 0;
+    if (B < 0 || L < 0 || D < 0 || !io_ok(io)) return 0;
+    if (B == 0 || L == 0 || D == 0) return lr::kStatusBytes;
     lr::DiagPlan p;
     if (lr::minmax_plan(B, L, D, io, &p) != LR_OK) return SIZE_MAX;
     return p.ws_bytes;
@@ -323,8 +384,11 @@ extern "C" int lr_minmax_scan_fwd(const void *r, const void *s, const float *x0,
     int rc = validate_minmax(r, s, x0, y, x_final, B, L, D, io);
     if (rc != LR_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (B == 0 || D == 0) return LR_OK;
-    if (L == 0) return copy_state(x0, x_final, size_t(B) * D, st);
+    if (B == 0 || D == 0) return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    if (L == 0) {
+        if ((rc = copy_state(x0, x_final, size_t(B) * D, st)) != LR_OK) return rc;
+        return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    }
     lr::DiagPlan p;
     if ((rc = lr::minmax_plan(B, L, D, io, &p)) != LR_OK) return rc;
     if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
@@ -341,8 +405,11 @@ extern "C" int lr_rglru_scan_preact_fwd(const void *x, const void *r_pre, const 
     int rc = validate_rglru(x, r_pre, i_pre, a_log, c, h0, y, h_final, B, L, D, io);
     if (rc != LR_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (B == 0 || D == 0) return LR_OK;
-    if (L == 0) return copy_state(h0, h_final, size_t(B) * D, st);
+    if (B == 0 || D == 0) return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    if (L == 0) {
+        if ((rc = copy_state(h0, h_final, size_t(B) * D, st)) != LR_OK) return rc;
+        return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    }
     lr::DiagPlan p;
     if ((rc = lr::rglru_plan(B, L, D, io, &p)) != LR_OK) return rc;
     if ((rc = check_workspace(p, workspace, ws_bytes)) != LR_OK) return rc;
@@ -361,14 +428,18 @@ extern "C" int lr_hgrn2_preact_fwd(const void *q, const void *k, const void *v, 
     int rc = validate_hgrn2(q, k, v, f, S0, o, S_final, B, L, H, dk, dv, chunk, io);
     if (rc != LR_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (B == 0) return LR_OK;
-    if (L == 0) return copy_state(S0, S_final, size_t(B) * H * dv * dk, st);
+    if (B == 0) return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    if (L == 0) {
+        if ((rc = copy_state(S0, S_final, size_t(B) * H * dv * dk, st)) != LR_OK) return rc;
+        return lr::status_ok_no_launch(workspace, ws_bytes, st);
+    }
     size_t need = 0;
     if ((rc = lr::hgrn2_workspace(B, L, H, &need)) != LR_OK) return rc;
-    if (need > 0 && (workspace == nullptr || ws_bytes < need)) return LR_ERR_WORKSPACE;
+    if (workspace == nullptr || ws_bytes < need) return LR_ERR_WORKSPACE;
+    if (misaligned(workspace)) return LR_ERR_MISALIGNED;
     if (!hgrn2_tensor_path(dk, dv, chunk, io))
         return lr::hgrn2_general_launch(q, k, v, f, S0, o, S_final, B, L, H, dk, dv, io == LR_BF16,
-                                        true, lb, st);
+                                        true, lb, workspace, st);
     return lr::hgrn2_launch(q, k, v, f, S0, o, S_final, B, L, H, workspace, st, true, lb);
 }
 

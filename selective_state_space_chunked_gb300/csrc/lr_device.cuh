@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "lr_internal.h"
 #include "lrscan.h"
 
 namespace lr {
@@ -174,6 +175,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy global-memory writes before later
+// async-proxy (TMA) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -188,6 +195,52 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// Polls a look-back flag until it is non-zero or the limit runs out; returns
+// the flag value (0 on timeout).
+__device__ __forceinline__ uint32_t poll_flag(const uint32_t *flag, uint64_t limit_ns) {
+    uint32_t v = ld_acquire_gpu(flag);
+    if (v != 0) return v;
+    const uint64_t t0 = globaltimer_ns();
+    while ((v = ld_acquire_gpu(flag)) == 0) {
+        if (globaltimer_ns() - t0 > limit_ns) return 0;
+        __nanosleep(100);
+    }
+    return v;
+}
+
+// ----------------------------------------------------------------------------
+// Per-call device status
+// ----------------------------------------------------------------------------
+// A call's device-side errors go to a 64-bit status word at the start of its
+// workspace.  The host draws a fresh 48-bit stamp for every call; the word
+// holds (stamp << 16) | (16-bit status code).  One thread of the launch
+// stamps the word with code 0 unless the same call has already recorded an
+// error there; a thread that detects an error installs (stamp, code) unless
+// the same call recorded one first.  So after the call the word describes
+// that call alone, whatever the memory held before, and no clearing launch
+// is needed.  Launches of one call that share a stamp (the host-buffer path
+// runs a call as several launches) keep the first error.
+__device__ __forceinline__ void status_begin(const StatusRef &s) {
+    if (s.word == nullptr) return;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(s.word);
+    while ((old >> 16) != s.stamp) {
+        const unsigned long long prev = atomicCAS(s.word, old, s.stamp << 16);
+        if (prev == old) break;
+        old = prev;
+    }
+}
+
+static __device__ __noinline__ void status_report(StatusRef s, int code) {
+    if (s.word == nullptr) return;
+    const unsigned long long want = (s.stamp << 16) | (static_cast<unsigned>(code) & 0xffffu);
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(s.word);
+    while (!((old >> 16) == s.stamp && (old & 0xffffu) != 0)) {
+        const unsigned long long prev = atomicCAS(s.word, old, want);
+        if (prev == old) break;
+        old = prev;
+    }
 }
 
 }  // namespace lr

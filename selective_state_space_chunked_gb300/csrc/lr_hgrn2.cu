@@ -50,10 +50,6 @@
 
 namespace lr {
 
-__device__ int g_hgrn2_status = 0;
-
-__device__ __forceinline__ void hg_report(int code) { atomicCAS(&g_hgrn2_status, 0, code); }
-
 namespace hg {
 constexpr int C = 64;          // chunk length
 constexpr int DK = 128;        // key channels per head
@@ -143,12 +139,13 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                        const float *__restrict__ S0, float *__restrict__ S_final,
                        __nv_bfloat16 *__restrict__ o, int L, int H, int n_chunks, float lb,
-                       uint64_t timeout_ns) {
+                       uint64_t timeout_ns, StatusRef sref) {
     using namespace hg;
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0 && blockIdx.x == 0) status_begin(sref);
     if ((smem_u32(sm) & 1023u) != 0) {  // swizzled tiles need a 1024-byte aligned base
-        if (tid == 0) hg_report(LR_ERR_CUDA);
+        if (tid == 0) status_report(sref, LR_ERR_CUDA);
         return;
     }
     const int blk = blockIdx.x;
@@ -200,7 +197,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             if (*abort_flag != 0) return false;
             if (globaltimer_ns() - t0 > timeout_ns) {
                 *abort_flag = 1;
-                hg_report(LR_ERR_TIMEOUT);
+                status_report(sref, LR_ERR_TIMEOUT);
                 return false;
             }
         }
@@ -345,7 +342,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             for (int u = 0; u < FSTEPS; ++u) loc[u] += off;
             const float l0 = L0F[i];
             const float m = 0.5f * (l0 + lc);
-            if (qt == 0 && !(l0 - lc <= kMaxSpread)) hg_report(LR_ERR_RANGE);
+            if (qt == 0 && !(l0 - lc <= kMaxSpread)) status_report(sref, LR_ERR_RANGE);
             float *e1 = E1 + bi * (C * RB);
 #pragma unroll
             for (int u = 0; u < FSTEPS; ++u) e1[e1_index(tb + u, i)] = ex2_approx(loc[u] - m);
@@ -572,12 +569,12 @@ bool hg_setup_once() {
 }  // namespace
 
 int hgrn2_workspace(int64_t, int64_t, int64_t, size_t *bytes) {
-    *bytes = 0;
+    *bytes = kStatusBytes;   // the call status only
     return LR_OK;
 }
 
 int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
-                 void *o, float *S_final, int64_t B, int64_t L, int64_t H, void *,
+                 void *o, float *S_final, int64_t B, int64_t L, int64_t H, void *workspace,
                  cudaStream_t stream, bool preact, float lb) {
     const uint64_t HK = uint64_t(H) * hg::DK, HV = uint64_t(H) * hg::DV;
     CUtensorMap mq, mk, mv, mg;
@@ -592,20 +589,8 @@ int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, con
     auto kern = preact ? hgrn2_chunk_kernel<true> : hgrn2_chunk_kernel<false>;
     kern<<<static_cast<unsigned>(grid), hg::THREADS, hg::SMEM, stream>>>(
         mq, mk, mv, mg, S0, S_final, static_cast<__nv_bfloat16 *>(o), static_cast<int>(L),
-        static_cast<int>(H), n_chunks, lb, timeout);
+        static_cast<int>(H), n_chunks, lb, timeout, call_status(workspace));
     return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
-}
-
-int hgrn2_status_read_and_clear(int *status) {
-    int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_hgrn2_status, sizeof(int)) != cudaSuccess) return LR_ERR_CUDA;
-    if (v != 0) {
-        const int zero = 0;
-        if (cudaMemcpyToSymbol(g_hgrn2_status, &zero, sizeof(int)) != cudaSuccess)
-            return LR_ERR_CUDA;
-    }
-    *status = v;
-    return LR_OK;
 }
 
 }  // namespace lr

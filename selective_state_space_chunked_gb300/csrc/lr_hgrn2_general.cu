@@ -41,8 +41,6 @@ namespace {
 constexpr int kNT = 64;   // threads per block
 constexpr int kNB = 3;    // staging buffers: copies run two chunks ahead
 
-__device__ int g_hgrn2_gen_status = 0;
-
 // P lanes of CPT key columns share RT value rows
 template <int P, int CPT, int RT>
 struct GenCfg {
@@ -89,7 +87,7 @@ __global__ void __launch_bounds__(kNT, 1)
                          const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                          const IO *__restrict__ g, const float *__restrict__ S0,
                          IO *__restrict__ o, float *__restrict__ S_final, int L, int H, int dk,
-                         int dv, int nrb, float lb, uint64_t timeout_ns) {
+                         int dv, int nrb, float lb, uint64_t timeout_ns, StatusRef sref) {
     using C = GenCfg<P, CPT, RT>;
     constexpr int kCPT = CPT, kRT = RT;
     constexpr int KB = C::KB, RB = C::RB, TC = C::TC, VT = C::VT;
@@ -103,6 +101,7 @@ __global__ void __launch_bounds__(kNT, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(os + VT);    // [NB]: chunk staged
 
     const int tid = threadIdx.x;
+    if (tid == 0 && blockIdx.x == 0) status_begin(sref);
     const int p = tid % P, rg = tid / P;
     const int bh = blockIdx.x / nrb, rb = blockIdx.x - bh * nrb;
     const int b = bh / H, h = bh - b * H;
@@ -201,7 +200,7 @@ __global__ void __launch_bounds__(kNT, 1)
         const bool ok = !TMA || mbar_wait_bounded(&full[buf], (c / kNB) & 1, timeout_ns);
         if (__syncthreads_or(!ok)) {   // chunk c never arrived: report and stop
             if (tid == 0) {
-                atomicCAS(&g_hgrn2_gen_status, 0, LR_ERR_TIMEOUT);
+                status_report(sref, LR_ERR_TIMEOUT);
                 // let the copies already issued land (bounded) before the block exits
                 for (int c2 = c + 1; c2 < c + kNB && c2 < nchunks; ++c2)
                     mbar_wait_bounded(&full[c2 % kNB], (c2 / kNB) & 1, timeout_ns);
@@ -276,7 +275,7 @@ inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr
 template <typename IO, int P, int CPT, int RT>
 int launch_p(const void *q, const void *k, const void *v, const void *g, const float *S0, void *o,
              float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv, bool pre,
-             float lb, cudaStream_t stream) {
+             float lb, StatusRef st, cudaStream_t stream) {
     using C = GenCfg<P, CPT, RT>;
     const int nrb = static_cast<int>((dv + C::RB - 1) / C::RB);
     const int64_t grid = B * H * nrb;
@@ -306,7 +305,7 @@ int launch_p(const void *q, const void *k, const void *v, const void *g, const f
         mq, mk, mv, mg, static_cast<const IO *>(q), static_cast<const IO *>(k),
         static_cast<const IO *>(v), static_cast<const IO *>(g), S0, static_cast<IO *>(o), S_final,
         static_cast<int>(L), static_cast<int>(H), static_cast<int>(dk), static_cast<int>(dv), nrb, lb,
-        kDefaultTimeoutNs);
+        kDefaultTimeoutNs, st);
     return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 
@@ -315,18 +314,18 @@ int launch_p(const void *q, const void *k, const void *v, const void *g, const f
 template <typename IO, int DKP>
 int launch_dk(const void *q, const void *k, const void *v, const void *g, const float *S0, void *o,
               float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv, bool pre,
-              float lb, cudaStream_t stream) {
+              float lb, StatusRef st, cudaStream_t stream) {
     int sms = 0;
     if (device_sm_count(&sms) != LR_OK) return LR_ERR_CUDA;
     auto blocks = [&](int rb) { return B * H * ((dv + rb - 1) / rb); };
     const int64_t want = 3 * int64_t(sms) / 2;
     if (DKP > 256 || blocks(2 * kNT / (DKP / 32)) >= want)
-        return launch_p<IO, DKP / 32, 32, 2>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, stream);
+        return launch_p<IO, DKP / 32, 32, 2>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
     if constexpr (DKP <= 256) {
         if (blocks(kNT / (DKP / 32)) >= want)
             return launch_p<IO, DKP / 32, 32, 1>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb,
-                                                 stream);
-        return launch_p<IO, DKP / 16, 16, 1>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, stream);
+                                                 st, stream);
+        return launch_p<IO, DKP / 16, 16, 1>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
     }
     return LR_ERR_UNSUPPORTED;
 }
@@ -334,34 +333,25 @@ int launch_dk(const void *q, const void *k, const void *v, const void *g, const 
 template <typename IO>
 int launch_io(const void *q, const void *k, const void *v, const void *g, const float *S0, void *o,
               float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
-              bool pre, float lb, cudaStream_t stream) {
-    if (dk <= 32) return launch_dk<IO, 32>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, stream);
-    if (dk <= 64) return launch_dk<IO, 64>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, stream);
-    if (dk <= 128) return launch_dk<IO, 128>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, stream);
-    if (dk <= 256) return launch_dk<IO, 256>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, stream);
-    return launch_dk<IO, 512>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, stream);
+              bool pre, float lb, StatusRef st, cudaStream_t stream) {
+    if (dk <= 32) return launch_dk<IO, 32>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
+    if (dk <= 64) return launch_dk<IO, 64>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
+    if (dk <= 128) return launch_dk<IO, 128>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
+    if (dk <= 256) return launch_dk<IO, 256>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
+    return launch_dk<IO, 512>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
 }
 
 }  // namespace
 
 int hgrn2_general_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                          void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
-                         int64_t dv, int io_bf16, bool preact, float lb, cudaStream_t stream) {
+                         int64_t dv, int io_bf16, bool preact, float lb, void *workspace,
+                         cudaStream_t stream) {
     if (B * H * dv == 0) return LR_OK;
+    const StatusRef st = call_status(workspace);
     return io_bf16 ? launch_io<__nv_bfloat16>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, preact, lb,
-                                              stream)
-                   : launch_io<float>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, preact, lb, stream);
-}
-
-int hgrn2_general_status_read_and_clear(int *status) {
-    int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_hgrn2_gen_status, sizeof(int)) != cudaSuccess) return LR_ERR_CUDA;
-    if (v != 0) {
-        const int zero = 0;
-        if (cudaMemcpyToSymbol(g_hgrn2_gen_status, &zero, sizeof(int)) != cudaSuccess) return LR_ERR_CUDA;
-    }
-    *status = v;
-    return LR_OK;
+                                              st, stream)
+                   : launch_io<float>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, preact, lb, st, stream);
 }
 
 }  // namespace lr

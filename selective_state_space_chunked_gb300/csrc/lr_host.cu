@@ -75,8 +75,9 @@ bool copy_rows(void *dst, size_t dpitch, const void *src, size_t spitch, size_t 
     return true;
 }
 
-// Workspace layout: parameters, two states, the kernel workspace, then two
-// input and two output staging buffers (every region 256-byte aligned).
+// Workspace layout: the kernel workspace (so its call status sits at the
+// start of the whole workspace), parameters, two states, then two input and
+// two output staging buffers (every region 256-byte aligned).
 struct Layout {
     size_t par[3] = {}, state[2] = {}, kws = 0, in_buf[2] = {}, out_buf[2] = {};
     size_t in_off[6] = {}, out_off[2] = {}, in_bytes = 0, out_bytes = 0, total = 0;
@@ -85,6 +86,8 @@ struct Layout {
 Layout layout(const HostJob &j) {
     Layout l;
     size_t at = 0;
+    l.kws = at;
+    at += al256(j.kernel_ws);
     for (int p = 0; p < j.n_par; ++p) {
         l.par[p] = at;
         at += al256(j.par[p].bytes);
@@ -93,8 +96,6 @@ Layout layout(const HostJob &j) {
         l.state[s] = at;
         at += al256(j.state_bytes);
     }
-    l.kws = at;
-    at += al256(j.kernel_ws);
     for (int i = 0; i < j.n_in; ++i) {
         l.in_off[i] = l.in_bytes;
         l.in_bytes += al256(size_t(j.B) * j.Lc * j.in[i].width * j.es);
@@ -159,6 +160,7 @@ int run_host_job(const HostJob &j, void *workspace, size_t ws_bytes, cudaStream_
              cudaSuccess;
 
     int rc = LR_OK;
+    const SharedStamp one_call;   // every chunk launch records into the same call status
     const int64_t K = (j.L + j.Lc - 1) / j.Lc;
     for (int64_t k = 0; k < K && ok && rc == LR_OK; ++k) {
         const int b = int(k & 1);
@@ -203,7 +205,11 @@ int run_host_job(const HostJob &j, void *workspace, size_t ws_bytes, cudaStream_
                         cudaStreamSynchronize(r->s_comp) == cudaSuccess &&
                         cudaStreamSynchronize(r->s_out) == cudaSuccess;
     if (rc != LR_OK) return rc;
-    return ok && synced ? LR_OK : LR_ERR_CUDA;
+    if (!(ok && synced)) return LR_ERR_CUDA;
+    // the chunks' device-side status (a bounded wait that ran out)
+    int code = LR_OK;
+    if (read_status(ws + lay.kws, r->s_comp, &code, false) != LR_OK) return LR_ERR_CUDA;
+    return code;
 }
 
 }  // namespace lr

@@ -11,6 +11,36 @@
 
 namespace lr {
 
+// Every workspace starts with this many bytes of call status (the 64-bit
+// status word at offset 0, the rest reserved), then the kernel's scratch.
+constexpr size_t kStatusBytes = 256;
+
+// Where a launch records device-side errors, and the call's stamp (see
+// status_begin / status_report in lr_device.cuh).
+struct StatusRef {
+    unsigned long long *word;   // NULL: the launch records nothing
+    unsigned long long stamp;   // 48-bit, non-zero
+};
+
+// A fresh stamp for a call (or the stamp of the enclosing host-buffer call,
+// whose chunk launches share one) with the status word at the start of
+// `workspace` (NULL: nothing recorded).
+StatusRef call_status(void *workspace);
+
+// Runs the calls made by this thread under one stamp while it lives.
+struct SharedStamp {
+    SharedStamp();
+    ~SharedStamp();
+};
+
+// Reads the status code recorded in a workspace's status word, in the order
+// of `stream` (it synchronises `stream`); `clear` resets the code to LR_OK.
+int read_status(void *workspace, cudaStream_t stream, int *code, bool clear = false);
+
+// Records LR_OK for a call that launches nothing (an empty problem), so the
+// workspace's status word describes that call.
+int status_ok_no_launch(void *workspace, size_t ws_bytes, cudaStream_t stream);
+
 // Work decomposition of a diagonal scan (selective or RG-LRU).
 //   n_cb   channel blocks (batch x ceil(D / DC)); one thread block each when S == 1
 //   S      time splits per channel block (S > 1: decoupled look-back between splits)
@@ -23,7 +53,9 @@ struct DiagPlan {
     int dc = 0;           // channels per thread block
     int tile_t = 0;       // time steps per tile
     size_t ctrl_bytes = 0;  // flags + ticket (cleared at each call)
-    size_t ws_bytes = 0;    // total workspace
+    size_t ws_bytes = 0;    // total workspace, status bytes included
+    int warps = 0;          // selective scan: warps sharing the flat tile list
+    int grid = 0;           // selective scan: thread blocks
 };
 
 // Process-wide knobs (see lr_set_split_override / lr_test_withhold_split).
@@ -53,9 +85,8 @@ int minmax_launch(const void *r, const void *s, const float *x0, void *y, float 
                   int64_t L, int64_t D, lr_dtype io, const DiagPlan &p, void *workspace,
                   cudaStream_t stream);
 
-int diag_status_read_and_clear(int *status);
-
-// Built-in scratch of lr_rglru_scan_fwd_noalloc (1 MiB per device).
+// Built-in scratch of lr_rglru_scan_fwd_noalloc (1 MiB per device; its first
+// kStatusBytes hold the call status).
 constexpr size_t kRglruScratchBytes = size_t(1) << 20;
 int rglru_builtin_scratch(void **ptr);  // device address, set up once per device
 
@@ -64,17 +95,16 @@ int hgrn2_workspace(int64_t B, int64_t L, int64_t H, size_t *bytes);
 int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                  void *o, float *S_final, int64_t B, int64_t L, int64_t H, void *workspace,
                  cudaStream_t stream, bool preact = false, float lb = 0.0f);
-int hgrn2_status_read_and_clear(int *status);
 // 3-D TMA map over a row-major (d2, d1, d0) tensor with a (b0, b1, b2) box,
 // no swizzle, zero fill outside the tensor; false if the driver refuses it.
 bool encode_map_3d(CUtensorMap *tm, const void *base, CUtensorMapDataType type, size_t esize,
                    uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2);
 
 // HGRN2 for fp32 I/O and head dims other than 128 x 128 (CUDA cores, step by step)
-int hgrn2_general_status_read_and_clear(int *status);
 int hgrn2_general_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                          void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
-                         int64_t dv, int io_bf16, bool preact, float lb, cudaStream_t stream);
+                         int64_t dv, int io_bf16, bool preact, float lb, void *workspace,
+                         cudaStream_t stream);
 
 // Single-token decode steps (plain one-pass kernels)
 int selective_step_launch(const void *x, const void *dt, const void *z, const void *Bm, const void *Cm,

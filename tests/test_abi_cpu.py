@@ -128,11 +128,25 @@ def test_hgrn2_validation_codes(lr, kw, code):
     assert call_hg(lr, **kw) == code
 
 
-def test_workspace_size_degenerate_shapes_need_nothing(lr):
-    assert lr.lr_selective_scan_workspace_size(0, 10, 64, 16, 1) == 0
-    assert lr.lr_selective_scan_workspace_size(1, 10, 64, 8, 1) == 0
-    assert lr.lr_rglru_scan_workspace_size(1, 0, 64, 1) == 0
-    assert lr.lr_hgrn2_workspace_size(1, 0, 2, 128, 128, 1) == 0
+def test_workspace_size_of_empty_problems_is_the_call_status(lr):
+    """Every call's device status lives in its workspace's first 256 bytes,
+    so even an empty problem (nothing launched) asks for them; invalid
+    arguments ask for nothing."""
+    assert lr.lr_selective_scan_workspace_size(0, 10, 64, 16, 1) == 256
+    assert lr.lr_selective_scan_workspace_size(1, 10, 64, 8, 1) == 0     # N != 16
+    assert lr.lr_selective_scan_workspace_size(-1, 10, 64, 16, 1) == 0
+    assert lr.lr_rglru_scan_workspace_size(1, 0, 64, 1) == 256
+    assert lr.lr_minmax_scan_workspace_size(1, 4, 0, 1) == 256
+    assert lr.lr_hgrn2_workspace_size(1, 0, 2, 128, 128, 1) == 256
+    assert lr.lr_hgrn2_workspace_size(1, 0, 0, 128, 128, 1) == 0         # H == 0
+
+
+def test_hgrn2_needs_a_workspace_for_its_status(lr):
+    """HGRN2 keeps its device status (LR_ERR_RANGE / LR_ERR_TIMEOUT) in the
+    caller's workspace like the other scans: no workspace, no call."""
+    rc = lr.lr_hgrn2_fwd(FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 4, 2, 128, 128, 64, 1,
+                         None, 0, None)
+    assert rc == lr.LR_ERR_WORKSPACE
 
 
 def test_hidden_not_divisible_by_heads_raises_value_error(lr):

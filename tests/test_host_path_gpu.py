@@ -77,7 +77,7 @@ def test_hgrn2_host_path(lr, chunk, io, dk):
     S0 = 0.1 * p["S0"]
     o, Sf = lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=2, S0=S0)
     orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], 2, S0=S0)
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     assert rel_err(o.float(), orf) <= TOL[io] and rel_err(Sf, Srf) <= TOL[io]
 
 

@@ -36,7 +36,7 @@ def _free(lr):
     yield
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
 
 
 def channels(D, seed):

@@ -40,7 +40,7 @@ def _clean_knobs(lr):
     yield
     lr.lr_set_split_override(0)
     lr.lr_test_withhold_split(-1, 1000)
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
 
 
 def cuda(d):
@@ -232,7 +232,11 @@ def test_selective_lattice_large_steps(lr, io):
 
 def test_selective_bf16_B4_L16384_D4096_sampled_and_four_segments(lr):
     """B=4, L=16384, d_inner=4096, N=16, bf16 I/O, h0 ~ N(0,1); also run as 4
-    segments of 4096 carried through the final state."""
+    segments of 4096 carried through the final state.  The kernel cuts each
+    launch's sequences into pieces of its own (a whole-GPU partition that
+    depends on L), so the segmented run rounds differently from the single
+    run: the two agree within the bf16 output tolerance, and the carried fp32
+    state within the fp32 one."""
     cfg = wl.WORKLOADS["selective_bf16"]
     p = wl.make_inputs(cfg, device="cuda")
     args = (p["x"], p["dt"], p["Bm"], p["Cm"], p["A_log"])
@@ -261,8 +265,8 @@ def test_selective_bf16_B4_L16384_D4096_sampled_and_four_segments(lr):
                                   Dskip=p["Dskip"], h0=h)
         segs.append(yk)
     torch.cuda.synchronize()
-    assert torch.equal(torch.cat(segs, 1), y)
-    assert torch.equal(h, hf)
+    assert rel_err(torch.cat(segs, 1).float().cpu(), y.float().cpu()) <= TOL["bf16"]
+    assert rel_err(h.cpu(), hf.cpu()) <= TOL["f32"]
 
 
 def test_selective_bf16_B4_L16384_D4096_general_decays_sampled(lr):
@@ -314,14 +318,14 @@ def test_bounded_lookback_wait_reports_timeout_and_recovers(lr):
     lr.lr_set_split_override(4)
     lr.lr_test_withhold_split(1, 50)
     run_rglru(lr, p)
-    assert lr.lr_check_status(0) == lr.LR_ERR_TIMEOUT
-    assert lr.lr_check_status(0) == 0  # read-and-clear
+    assert lr.status() == lr.LR_ERR_TIMEOUT
+    assert lr.status() == 0  # read-and-clear
     lr.lr_test_withhold_split(-1, 1000)
     check_rglru(lr, p, "f32")
     # same for the selective scan
     q = wl.selective_inputs(1, 400, 32, seed=4, io="f32", with_h0=True)
     lr.lr_test_withhold_split(2, 50)
     run_sel(lr, q)
-    assert lr.lr_check_status(0) == lr.LR_ERR_TIMEOUT
+    assert lr.status() == lr.LR_ERR_TIMEOUT
     lr.lr_test_withhold_split(-1, 1000)
     check_sel(lr, q, "f32")

@@ -32,7 +32,7 @@ def test_minmax_bf16_B8_L4096_D2560_sampled_exact(lr):
     x0 = torch.randn(B, D, device="cuda", generator=g).to(torch.bfloat16).float()
     y, xf = lr.minmax_scan(r, s, x0)
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     rng = np.random.default_rng(3)
     for b in (0, B - 1):
         ds = torch.from_numpy(np.concatenate([np.sort(rng.choice(D, 40, replace=False)), [0, D - 1]])).cuda()
@@ -61,7 +61,7 @@ def test_hgrn2_preact_bf16_B4_L4096_H16_sampled(lr):
     p = wl.make_inputs(cfg, device="cuda")
     o, Sf = lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=cfg.H, gate_lb=0.2)
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     for b, h in ((0, 0), (3, 15)):
         sl = slice(h * 128, (h + 1) * 128)
         sub = {n: p[n][b:b + 1, :, sl].cpu() for n in ("q", "k", "v", "g")}
@@ -78,7 +78,7 @@ def test_hgrn2_f32_B4_L4096_H16_general_kernel_sampled(lr):
     del p
     o, Sf = lr.hgrn2(pf["q"], pf["k"], pf["v"], pf["g"], H=cfg.H)
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     for b, h in ((1, 3), (2, 12)):
         sl = slice(h * 128, (h + 1) * 128)
         sub = {n: pf[n][b:b + 1, :, sl].cpu() for n in ("q", "k", "v", "g")}

@@ -34,7 +34,7 @@ def run(lr, p, S0=None):
     q, k, v, g = (p[n].cuda() for n in ("q", "k", "v", "g"))
     o, Sf = lr.hgrn2(q, k, v, g, H=p["H"], S0=None if S0 is None else S0.cuda())
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     return o.float().cpu(), Sf.cpu()
 
 
@@ -85,8 +85,8 @@ def test_hgrn2_gate_spread_beyond_range_is_reported(lr):
     p["g"] = torch.full_like(p["g"], 0.1)   # 64 steps of log2(0.1) = -212
     q, k, v, g = (p[n].cuda() for n in ("q", "k", "v", "g"))
     lr.hgrn2(q, k, v, g, H=1)
-    assert lr.lr_check_status(0) == lr.LR_ERR_RANGE
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == lr.LR_ERR_RANGE
+    assert lr.status() == 0
 
 
 def test_hgrn2_bf16_B4_L4096_H16_sampled(lr):
@@ -95,7 +95,7 @@ def test_hgrn2_bf16_B4_L4096_H16_sampled(lr):
     p = wl.make_inputs(cfg, device="cuda")
     o, Sf = lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=cfg.H)
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     for b, h in ((0, 0), (3, 15), (1, 7)):
         sl = slice(h * 128, (h + 1) * 128)
         sub = {n: p[n][b:b + 1, :, sl].cpu() for n in ("q", "k", "v", "g")}
@@ -127,7 +127,7 @@ def test_hgrn2_general_path_matches_oracle(lr, dtype, tol, B, L, H, dk, dv):
     S0 = 0.1 * torch.randn(B, H, dv, dk, generator=torch.Generator().manual_seed(L))
     o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), p["g"].cuda(), H=H, S0=S0.cuda())
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], H, S0=S0)
     assert rel_err(o.float().cpu(), orf) <= tol
     assert rel_err(Sf.cpu(), Srf) <= tol
@@ -157,7 +157,7 @@ def test_hgrn2_general_path_fast_decay_has_no_range_limit(lr):
     p["g"] = torch.full_like(p["g"], 0.1)
     o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), p["g"].cuda(), H=1)
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], 1)
     assert rel_err(o.cpu(), orf) <= 1e-4 and rel_err(Sf.cpu(), Srf) <= 1e-4
 
@@ -178,7 +178,7 @@ def test_hgrn2_general_path_wide_grids(lr, dtype, tol, B, L, H):
     else:
         o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), p["g"].cuda(), H=H)
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], H)
     assert rel_err(o.float().cpu(), orf) <= tol
     assert rel_err(Sf.cpu(), Srf) <= tol

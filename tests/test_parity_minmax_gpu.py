@@ -42,7 +42,7 @@ def inputs(B, L, D, seed, io, with_x0=True):
 def check(lr, r, s, x0):
     y, xf = lr.minmax_scan(r.cuda(), s.cuda(), None if x0 is None else x0.cuda())
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     yr, xr = oracle.minmax_scan(r, s, x0)
     yg = y.double().cpu().numpy()
     assert np.array_equal(yg, yr, equal_nan=True)
@@ -94,8 +94,8 @@ def test_minmax_bounded_lookback_wait_reports_timeout(lr):
     lr.lr_test_withhold_split(1, 50)
     try:
         lr.minmax_scan(r.cuda(), s.cuda(), x0.cuda())
-        assert lr.lr_check_status(0) == lr.LR_ERR_TIMEOUT
-        assert lr.lr_check_status(0) == 0
+        assert lr.status() == lr.LR_ERR_TIMEOUT
+        assert lr.status() == 0
     finally:
         lr.lr_test_withhold_split(-1, 1000)
         lr.lr_set_split_override(0)
@@ -108,7 +108,7 @@ def test_minmax_full_size_sampled(lr):
     r, s, x0 = inputs(8, 4096, 2560, seed=9, io="bf16")
     y, xf = lr.minmax_scan(r.cuda(), s.cuda(), x0.cuda())
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     for b in (0, 7):
         ch = torch.arange(0, 2560, 37)
         yr, xr = oracle.minmax_scan(r[b:b + 1, :, ch], s[b:b + 1, :, ch], x0[b:b + 1, ch])

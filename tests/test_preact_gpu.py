@@ -65,7 +65,7 @@ def test_hgrn2_preact_matches_oracle(lr, B, L, H, lb):
     f = torch.randn(B, L, H * 128, generator=torch.Generator().manual_seed(L)).add(2.0).to(torch.bfloat16)
     o, Sf = lr.hgrn2(p["q"].cuda(), p["k"].cuda(), p["v"].cuda(), f.cuda(), H=H, gate_lb=lb)
     torch.cuda.synchronize()
-    assert lr.lr_check_status(0) == 0
+    assert lr.status() == 0
     gate = lb + (1.0 - lb) * torch.sigmoid(f.double())
     orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], gate, H)
     assert rel_err(o.float().cpu(), orf) <= 1e-2
