@@ -113,11 +113,20 @@ int lr_check_status(void *workspace, lr_stream_t stream);
  *
  * Decays: where A_log sits on the multi-scale initialisation lattice
  * (MultiScaleSSM.__init__: A[n] = (n+1) A[0], to 2^-20 relative in fp32 for
- * every state of every channel of a 16-channel warp, which the kernel checks
+ * every state of the 64 channels a warp holds, which the kernel checks
  * itself) the 16 decays of a step are computed as powers of exp(delta A[0]);
  * elsewhere as one exp per state.  The two forms differ by rounding only
  * (well inside max|y - y_exact| <= 1e-4 max|y_exact| for fp32 I/O and 1e-2
  * for bf16 I/O); the caller chooses nothing.
+ *
+ * Parallel pieces: the kernel cuts each sequence into pieces that run in
+ * parallel.  A piece that starts inside the sequence rebuilds its starting
+ * state from the preceding steps back to where the carried state has decayed
+ * below 2^-12 (bf16 I/O) or 2^-32 (fp32 I/O) of its size, or takes it from
+ * the preceding pieces (see lr_set_selective_warmup); the history left out
+ * is below that share, inside the tolerances above.  Results therefore
+ * depend on the rounding of the piece boundaries, which depend on the
+ * device's SM count and on B, L, D.
  *
  * Layouts: x, dt, z, y: (B, L, D) in `io`; Bm, Cm: (B, L, N) in `io`;
  *          A_log: (D, N) fp32; Dskip: (D) fp32; h0, h_final: (B, D, N) fp32.
@@ -417,6 +426,21 @@ int lr_hgrn2_step(const void *q, const void *k, const void *v, const void *g,
  * not thread-safe.  Returns the previous value.
  */
 int lr_set_split_override(int splits);
+
+/*
+ * Tuning / test knob of the selective scan.  The kernel cuts sequences into
+ * pieces that run in parallel.  A piece that starts inside a sequence first
+ * rebuilds the state reached just before it from the preceding steps, back
+ * to where every channel's slowest decay has fallen below 2^-12 (bf16 I/O) or
+ * 2^-32 (fp32 I/O), so that the history left out contributes less than that
+ * share of the state's size (a "warm-up"), when that window lies within
+ * `max_steps` steps; otherwise it runs from zero, takes its carry from the
+ * preceding pieces by decoupled look-back and corrects its outputs by the
+ * carry's contribution (to the same cut-off).  0 disables the warm-up (every
+ * carry by look-back).  Default 2048.  Process-wide, not thread-safe.
+ * Returns the previous setting.
+ */
+int64_t lr_set_selective_warmup(int64_t max_steps);
 
 /*
  * Tuning / test knob: the chunk length (time steps) of the host-buffer entry

@@ -40,6 +40,7 @@ SIGNATURES = {
     "lr_set_split_override": (_I, [_I]),
     "lr_test_withhold_split": (_I, [_I, _I]),
     "lr_set_host_chunk_steps": (_I64, [_I64]),
+    "lr_set_selective_warmup": (_I64, [_I64]),
     "lr_selective_scan_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I]),
     "lr_selective_scan_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I64, _I64, _I64, _I64, _I, _I, _P, _SZ, _P]),
@@ -126,6 +127,12 @@ def lr_set_split_override(splits: int) -> int:
 def lr_set_host_chunk_steps(steps: int) -> int:
     """Chunk length of the host-buffer path (0 = automatic); returns the previous."""
     return int(_lib.lr_set_host_chunk_steps(int(steps)))
+
+
+def lr_set_selective_warmup(max_steps: int) -> int:
+    """Longest warm-up of the selective scan's pieces (0 = carries by
+    look-back only); returns the previous setting."""
+    return int(_lib.lr_set_selective_warmup(int(max_steps)))
 
 
 def lr_test_withhold_split(split: int, timeout_ms: int = 1000) -> int:

@@ -16,6 +16,7 @@ namespace lr {
 int g_split_override = 0;
 int g_withheld_split = -1;
 int g_withheld_timeout_ms = 1000;
+int64_t g_selective_warmup_steps = 2048;
 
 namespace {
 std::atomic<unsigned long long> g_stamp{0};
@@ -204,6 +205,12 @@ int lr_set_split_override(int splits) {
 int64_t lr_set_host_chunk_steps(int64_t steps) {
     const int64_t prev = lr::g_host_chunk_override;
     lr::g_host_chunk_override = steps > 0 ? steps : 0;
+    return prev;
+}
+
+int64_t lr_set_selective_warmup(int64_t max_steps) {
+    const int64_t prev = lr::g_selective_warmup_steps;
+    lr::g_selective_warmup_steps = max_steps > 0 ? (max_steps < (int64_t(1) << 30) ? max_steps : (int64_t(1) << 30)) : 0;
     return prev;
 }
 

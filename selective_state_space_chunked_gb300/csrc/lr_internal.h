@@ -62,6 +62,7 @@ struct DiagPlan {
 extern int g_split_override;
 extern int g_withheld_split;
 extern int g_withheld_timeout_ms;
+extern int64_t g_selective_warmup_steps;   // lr_set_selective_warmup
 
 // Default wall-clock limit of every bounded device-side wait.
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s

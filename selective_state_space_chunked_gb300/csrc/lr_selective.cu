@@ -19,18 +19,31 @@
 // how long a piece's carry correction runs depends on its channels' decay
 // rates, and mixing channel groups spreads that work evenly over the SMs.
 //
-// A piece that starts inside a chain runs from a zero state.  Its carry-in,
+// A piece that starts inside a chain needs the state its chain reaches just
+// before it.  Because every state decays, that state depends, to any given
+// relative accuracy, only on a window of preceding steps: the piece first
+// walks back over them (the "warm-up"), summing their contributions
+//   h_{s-1}[n] = sum_t exp(A[n] (Lambda_{s-1} - Lambda_t)) delta_t B_t[n] x_t
+// from the latest step back -- each term independent of the others, so no
+// serial chain -- until, for every channel of the warp, the slowest decay
+// over the walked steps has fallen below 2^-c, or until the chain start (the
+// initial state, decayed over the whole prefix, is then added and the state
+// is exact).  The omitted history contributes less than 2^-c of the size the
+// state had at the window start: c = 32 for fp32 outputs, 12 for bf16
+// outputs (at the level of their rounding, far inside the bf16 tolerance).
+// The warm-up reads each window's x, dt, B_t once more (about one tenth of
+// the data for the pages' sequences) but never waits for another warp.
+//
+// When the window would exceed a limit (lr_set_selective_warmup; slow decays
+// or tiny steps), the piece instead runs from a zero state and its carry-in,
 // the state at the end of the preceding piece, arrives afterwards through a
 // decoupled look-back over the preceding warps' piece descriptors (Merrill &
 // Garland, "Single-pass Parallel Prefix Scan with Decoupled Look-back",
 // 2016), compressed to (sum of delta, h[16]) per channel because the decay of
 // state n over a range is exp(A[n] * sum of delta).  The piece's outputs are
 // then corrected in place, y_t += silu(z_t) sum_n C_t[n] exp(A[n] Lambda_t)
-// carry[n] with Lambda_t the sum of delta from the piece start to t, and the
-// correction stops once exp(max_n A[n] Lambda_t) < 2^-c for every channel of
-// the warp, so that every remaining term is below 2^-c of its value at the
-// piece start: c = 32 for fp32 outputs (256 times under fp32 rounding), 16
-// for bf16 outputs (128 times under the bf16 rounding of the outputs).
+// carry[n] with Lambda_t the sum of delta from the piece start to t, until
+// every remaining term is below 2^-c of its value at the piece start.
 //
 // Data movement.  Each warp streams its tiles through a private ring of
 // shared-memory stages filled by TMA (one lane issues the copies of x, dt, z,
@@ -66,6 +79,7 @@
 #ifndef LR_SEL_MINB2_BF16
 #define LR_SEL_MINB2_BF16 4
 #endif
+
 #ifndef LR_SEL_CPL_F32
 #define LR_SEL_CPL_F32 2
 #endif
@@ -104,7 +118,7 @@ struct SelCfg {
     // with two channels per lane, 2 x 255 with four)
     static constexpr int MINB = CPL == 2 ? (sizeof(IO) == 2 ? LR_SEL_MINB2_BF16 : 3) : 2;
     // log2 of the relative size where the carry correction stops
-    static constexpr float CUT = sizeof(IO) == 2 ? -16.0f : -32.0f;
+    static constexpr float CUT = sizeof(IO) == 2 ? -12.0f : -32.0f;
     static_assert(CPL == 2 || CPL == 4, "two or four channels per lane");
     static_assert(kT % 8 == 0, "tiles of whole 8-step passes");
     static_assert(STAGE % 128 == 0 && SLOT_N % 128 == 0, "TMA destinations stay 128-byte aligned");
@@ -209,6 +223,7 @@ struct SelArgs {
     float *incl;            // [W][16][chain width]: state at the end of a warp's last piece
     StatusRef st;
     int withheld;           // test hook: pieces with this ordinal in their chain never publish
+    int warmup_tiles;       // longest warm-up (tiles); 0: carries always by look-back
     uint64_t timeout_ns;
 };
 
@@ -393,6 +408,76 @@ __device__ __forceinline__ void tile_scan(const unsigned char *st, const BCRows<
     }
 }
 
+// One tile of the backward warm-up of a piece that starts at step s: adds
+// the tile's steps' contributions to the state just before s,
+//   acc[n] += G_t^(n+1) u_t B_t[n]     (lattice; exp2(A2[n] S_t) in general)
+// with G_t = exp(A[0] S_t) and S_t the sum of delta over steps t+1 .. s-1,
+// which `lamb` carries in (the steps after this tile) and out (this tile
+// added).  Each step's term is independent of the others, so there is no
+// serial chain.  Every step of a tile before s lies inside the sequence.
+template <typename IO, int CPL, bool ACC, bool SP, bool LAT>
+__device__ __forceinline__ void tile_back(const unsigned char *st, const BCRows<IO> &bc, float2 (&acc)[CPL][8],
+                                          const float2 (&A2)[CPL][8], const Lane<CPL> &ln,
+                                          float2 (&lamb)[CPL / 2]) {
+    using Cf = SelCfg<IO, CPL>;
+    using V = Vec<IO, CPL>;
+    using R = typename V::raw;
+    constexpr int NP = CPL / 2;
+    const int lane = threadIdx.x & 31;
+    const R *xs = reinterpret_cast<const R *>(st) + lane;
+    const R *ds = reinterpret_cast<const R *>(st + Cf::OFF_DT) + lane;
+#pragma unroll
+    for (int q = kT - 1; q >= 0; --q) {
+        float2 xv[NP], dl[NP], u[NP], sa[NP];
+        V::get(xs[q * 32], xv);
+        V::get(ds[q * 32], dl);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            if (SP) dl[j] = softplus2<ACC>(dl[j]);
+            u[j] = __fmul2_rn(dl[j], xv[j]);
+            sa[j] = lamb[j];                       // S_t: the steps after t
+            lamb[j] = __fadd2_rn(lamb[j], dl[j]);
+        }
+        const float *brow = bc.b + q * BCRows<IO>::STRIDE;
+        float2 Pk[CPL], Mk[CPL], uu[CPL];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            uu[2 * j] = make_float2(u[j].x, u[j].x);
+            uu[2 * j + 1] = make_float2(u[j].y, u[j].y);
+            if (LAT) {
+                const float2 ar = __fmul2_rn(sa[j], ln.a20[j]);
+                const float2 ar2 = __fadd2_rn(ar, ar);
+                Pk[2 * j] = make_float2(ex2_approx(ar.x), ex2_approx(ar2.x));
+                Pk[2 * j + 1] = make_float2(ex2_approx(ar.y), ex2_approx(ar2.y));
+                Mk[2 * j] = make_float2(Pk[2 * j].y, Pk[2 * j].y);
+                Mk[2 * j + 1] = make_float2(Pk[2 * j + 1].y, Pk[2 * j + 1].y);
+            }
+        }
+#pragma unroll
+        for (int g4 = 0; g4 < kN / 4; ++g4) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(brow + 4 * g4);
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+                const int g = 2 * g4 + gg;
+                const float2 bp = gg ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) {
+                    float2 dec;
+                    if (LAT) {
+                        if (g > 0) Pk[k] = __fmul2_rn(Pk[k], Mk[k]);
+                        dec = Pk[k];
+                    } else {
+                        const float sk = (k & 1) ? sa[k / 2].y : sa[k / 2].x;
+                        const float2 ar = __fmul2_rn(make_float2(sk, sk), A2[k][g]);
+                        dec = make_float2(ex2_approx(ar.x), ex2_approx(ar.y));
+                    }
+                    acc[k][g] = __ffma2_rn(__fmul2_rn(uu[k], dec), bp, acc[k][g]);
+                }
+            }
+        }
+    }
+}
+
 // One tile of the carry correction of a piece: the TMA slot of x holds the
 // piece's outputs y.  lam accumulates delta from the piece start; cy = the
 // carry-in state.  y_t += silu(z_t) sum_n C_t[n] exp2(A2[n] lam_t) cy[n].
@@ -488,17 +573,25 @@ struct Ring {
 
 // Lane 0: copies tile t0 of chain (b, d0) into ring slot `slot`; slot 0 of
 // the stage gets x (scan) or y (correction).
-template <typename IO, int CPL, bool HAS_Z>
+// KIND 0: x (or y), dt, z, B, C; KIND 1: x, dt, B (the backward warm-up).
+template <typename IO, int CPL, bool HAS_Z, int KIND = 0>
 __device__ __forceinline__ void issue_tile(const Ring &rg, uint32_t slot, const CUtensorMap *m0, const Maps &m,
                                            int b, int d0, int t0) {
     using Cf = SelCfg<IO, CPL>;
     const uint32_t s = slot % Cf::STAGES;
     unsigned char *st = rg.base + s * Cf::STAGE;
     uint64_t *bar = &rg.full[s];
-    constexpr uint32_t bytes = uint32_t((HAS_Z ? 3 : 2) * Cf::SLOT + 2 * Cf::SLOT_N);
+    constexpr uint32_t bytes =
+        KIND == 1 ? uint32_t(2 * Cf::SLOT + Cf::SLOT_N) : uint32_t((HAS_Z ? 3 : 2) * Cf::SLOT + 2 * Cf::SLOT_N);
     // the lanes' generic reads of this stage's previous tile come first
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar, bytes);
+    if (KIND == 1) {
+        tma_load_3d(st, m.x, bar, d0, t0, b);
+        tma_load_3d(st + Cf::OFF_DT, m.dt, bar, d0, t0, b);
+        tma_load_3d(st + Cf::OFF_B, m.B, bar, 0, t0, b);
+        return;
+    }
     tma_load_3d(st, m0, bar, d0, t0, b);
     tma_load_3d(st + Cf::OFF_DT, m.dt, bar, d0, t0, b);
     if (HAS_Z) tma_load_3d(st + Cf::OFF_Z, m.z, bar, d0, t0, b);
@@ -513,27 +606,28 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64
     return __all_sync(kFull, ok);
 }
 
-// Streams tiles [v0, v1) of chain (b, d0) through the ring and calls
-// body(stage, bc, t0) for each; body returns false to stop early.  Tiles
-// already in flight when it stops are waited for, so no copy is pending when
-// the ring is reused or the warp exits.
-template <typename IO, int CPL, bool HAS_Z, typename Body>
+// Streams n tiles of chain (b, d0) through the ring -- v0, v0 + 1, ... (DIR
+// = 1) or v0, v0 - 1, ... (DIR = -1) -- and calls body(stage, bc, t0) for
+// each; body returns false to stop early.  Tiles already in flight when it
+// stops are waited for, so no copy is pending when the ring is reused or the
+// warp exits.  KIND 1 copies x, dt and B only.
+template <typename IO, int CPL, bool HAS_Z, int KIND = 0, int DIR = 1, typename Body>
 __device__ __forceinline__ void stream_tiles(Ring &rg, const CUtensorMap *m0, const Maps &m, int b, int d0,
-                                             int v0, int v1, uint64_t timeout_ns, const StatusRef &st,
+                                             int v0, int n, uint64_t timeout_ns, const StatusRef &st,
                                              Body &&body) {
     using Cf = SelCfg<IO, CPL>;
     const int lane = threadIdx.x & 31;
     float *bcf = reinterpret_cast<float *>(rg.base + Cf::OFF_BCF);
-    const int n = v1 - v0;
     if (n <= 0 || !rg.ok) return;
     const uint32_t it0 = rg.it;
     int issued = n < Cf::STAGES - 1 ? n : Cf::STAGES - 1;
     if (lane == 0)
-        for (int k = 0; k < issued; ++k) issue_tile<IO, CPL, HAS_Z>(rg, it0 + k, m0, m, b, d0, (v0 + k) * kT);
+        for (int k = 0; k < issued; ++k)
+            issue_tile<IO, CPL, HAS_Z, KIND>(rg, it0 + k, m0, m, b, d0, (v0 + DIR * k) * kT);
     int k = 0;
     while (k < n) {
         if (issued < n) {   // into the stage the previous tile released
-            if (lane == 0) issue_tile<IO, CPL, HAS_Z>(rg, it0 + issued, m0, m, b, d0, (v0 + issued) * kT);
+            if (lane == 0) issue_tile<IO, CPL, HAS_Z, KIND>(rg, it0 + issued, m0, m, b, d0, (v0 + DIR * issued) * kT);
             ++issued;
         }
         const uint32_t slot = it0 + k;
@@ -546,7 +640,7 @@ __device__ __forceinline__ void stream_tiles(Ring &rg, const CUtensorMap *m0, co
         }
         const unsigned char *stg = rg.base + s * Cf::STAGE;
         const BCRows<IO> bc = widen_bc<IO, CPL>(stg, bcf);
-        const bool go = body(stg, bc, (v0 + k - 1) * kT);
+        const bool go = body(stg, bc, (v0 + DIR * (k - 1)) * kT);
         __syncwarp();
         if (!go) break;
     }
@@ -558,6 +652,32 @@ __device__ __forceinline__ void stream_tiles(Ring &rg, const CUtensorMap *m0, co
         }
     }
     rg.it = it0 + issued;
+}
+
+template <int CPL>
+__device__ __forceinline__ void write_h_final(const SelArgs &a, const Lane<CPL> &ln, const float2 (&h)[CPL][8]) {
+    if (a.h_final == nullptr || !ln.valid) return;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        float4 *dst = reinterpret_cast<float4 *>(a.h_final + (size_t(ln.b) * a.D + ln.d + k) * kN);
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            dst[g] = make_float4(h[k][2 * g].x, h[k][2 * g].y, h[k][2 * g + 1].x, h[k][2 * g + 1].y);
+    }
+}
+
+template <int CPL>
+__device__ __forceinline__ void load_h0(const SelArgs &a, const Lane<CPL> &ln, float2 (&h)[CPL][8]) {
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.h0 + (size_t(ln.b) * a.D + ln.d + k) * kN);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float4 v = (a.h0 != nullptr && ln.valid) ? src[g] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            h[k][2 * g] = make_float2(v.x, v.y);
+            h[k][2 * g + 1] = make_float2(v.z, v.w);
+        }
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -572,7 +692,7 @@ __device__ __forceinline__ void scan_piece(Ring &rg, const Maps &m, const SelArg
     if (!LAT) load_A2<CPL>(a.A_log, ln, A2);
     IO *y = static_cast<IO *>(a.y);
     const bool full_ch = ln.d0 + 32 * CPL <= a.D;
-    stream_tiles<IO, CPL, HAS_Z>(rg, m.x, m, ln.b, ln.d0, lo, hi, a.timeout_ns, a.st,
+    stream_tiles<IO, CPL, HAS_Z>(rg, m.x, m, ln.b, ln.d0, lo, hi - lo, a.timeout_ns, a.st,
                                  [&](const unsigned char *stg, const BCRows<IO> &bc, int t0) {
                                      IO *yp = y + (size_t(ln.b) * a.L + t0) * a.D + ln.d;
                                      if (full_ch && t0 + kT <= a.L) {
@@ -585,6 +705,63 @@ __device__ __forceinline__ void scan_piece(Ring &rg, const Maps &m, const SelArg
                                      }
                                      return true;
                                  });
+}
+
+// The backward warm-up of a piece starting at tile lo: the state just before
+// it, summed over the preceding steps from the latest back (tile_back) until,
+// for every channel of the warp, the slowest decay since then has fallen
+// below 2^CUT -- the rest of the history then contributes less than that
+// share of its size -- or the chain start is reached (the initial state,
+// decayed over the whole range, is then added and the result is exact).
+// Returns false (h untouched) when `cap` tiles did not reach either.
+template <typename IO, int CPL, bool ACC, bool HAS_Z, bool SP, bool LAT>
+__device__ __forceinline__ bool warm_up(Ring &rg, const Maps &m, const SelArgs &a, const Lane<CPL> &ln, int lo,
+                                        int cap, float2 (&h)[CPL][8]) {
+    using Cf = SelCfg<IO, CPL>;
+    float2 A2[CPL][8], acc[CPL][8], lamb[CPL / 2];
+    if (!LAT) load_A2<CPL>(a.A_log, ln, A2);
+#pragma unroll
+    for (int k = 0; k < CPL; ++k)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) acc[k][g] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < CPL / 2; ++j) lamb[j] = make_float2(0.0f, 0.0f);
+    const int n = lo < cap ? lo : cap;
+    int walked = 0;
+    bool reached = false;
+    stream_tiles<IO, CPL, HAS_Z, 1, -1>(rg, m.x, m, ln.b, ln.d0, lo - 1, n, a.timeout_ns, a.st,
+                                        [&](const unsigned char *stg, const BCRows<IO> &bc, int) {
+                                            tile_back<IO, CPL, ACC, SP, LAT>(stg, bc, acc, A2, ln, lamb);
+                                            ++walked;
+                                            bool done = true;
+#pragma unroll
+                                            for (int j = 0; j < CPL / 2; ++j)
+                                                done = done && ln.a2min[j].x * lamb[j].x <= Cf::CUT &&
+                                                       ln.a2min[j].y * lamb[j].y <= Cf::CUT;
+                                            reached = __all_sync(kFull, done || !ln.valid);
+                                            return !reached;
+                                        });
+    if (!rg.ok || !(reached || walked == lo)) return false;
+    if (walked == lo) {
+        // the whole prefix: add the initial state decayed over it
+        float2 h0v[CPL][8];
+        if (LAT) load_A2<CPL>(a.A_log, ln, A2);
+        load_h0<CPL>(a, ln, h0v);
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const float lk = (k & 1) ? lamb[k / 2].y : lamb[k / 2].x;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                const float2 dec = make_float2(pow2_t<ACC>(A2[k][g].x * lk), pow2_t<ACC>(A2[k][g].y * lk));
+                acc[k][g] = __ffma2_rn(dec, h0v[k][g], acc[k][g]);
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < CPL; ++k)
+#pragma unroll
+        for (int g = 0; g < 8; ++g) h[k][g] = acc[k][g];
+    return true;
 }
 
 // The carry correction of tiles [lo, hi) of a chain, stopping once every
@@ -600,7 +777,7 @@ __device__ __forceinline__ void correct_piece(Ring &rg, const Maps &m, const Sel
     float2 lam[CPL / 2];
 #pragma unroll
     for (int j = 0; j < CPL / 2; ++j) lam[j] = make_float2(0.0f, 0.0f);
-    stream_tiles<IO, CPL, HAS_Z>(rg, m.y, m, ln.b, ln.d0, lo, hi, a.timeout_ns, a.st,
+    stream_tiles<IO, CPL, HAS_Z>(rg, m.y, m, ln.b, ln.d0, lo, hi - lo, a.timeout_ns, a.st,
                                  [&](const unsigned char *stg, const BCRows<IO> &bc, int t0) {
                                      IO *yp = y + (size_t(ln.b) * a.L + t0) * a.D + ln.d;
                                      if (full_ch && t0 + kT <= a.L) {
@@ -721,32 +898,6 @@ __device__ __forceinline__ void look_back(const SelArgs &a, int wi, const float2
         for (int g = 0; g < 8; ++g) carry[k][g] = acc_h[k][g];
 }
 
-template <int CPL>
-__device__ __forceinline__ void write_h_final(const SelArgs &a, const Lane<CPL> &ln, const float2 (&h)[CPL][8]) {
-    if (a.h_final == nullptr || !ln.valid) return;
-#pragma unroll
-    for (int k = 0; k < CPL; ++k) {
-        float4 *dst = reinterpret_cast<float4 *>(a.h_final + (size_t(ln.b) * a.D + ln.d + k) * kN);
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-            dst[g] = make_float4(h[k][2 * g].x, h[k][2 * g].y, h[k][2 * g + 1].x, h[k][2 * g + 1].y);
-    }
-}
-
-template <int CPL>
-__device__ __forceinline__ void load_h0(const SelArgs &a, const Lane<CPL> &ln, float2 (&h)[CPL][8]) {
-#pragma unroll
-    for (int k = 0; k < CPL; ++k) {
-        const float4 *src = reinterpret_cast<const float4 *>(a.h0 + (size_t(ln.b) * a.D + ln.d + k) * kN);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const float4 v = (a.h0 != nullptr && ln.valid) ? src[g] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            h[k][2 * g] = make_float2(v.x, v.y);
-            h[k][2 * g + 1] = make_float2(v.z, v.w);
-        }
-    }
-}
-
 // Warp owning flat tile f.
 __device__ __forceinline__ long long owner_of(long long f, long long F, int W) {
     return ((f + 1) * W + F - 1) / F - 1;
@@ -807,13 +958,21 @@ __global__ void __launch_bounds__(kWpb * 32, SelCfg<IO, CPL>::MINB)
 #pragma unroll
             for (int g = 0; g < 8; ++g) h[k][g] = make_float2(0.0f, 0.0f);
     }
+    // a piece that starts inside its chain first warms up its state over the
+    // preceding steps where the carry still counts, when that horizon is
+    // short enough; otherwise it runs from zero and takes its carry by
+    // look-back and correction below
+    bool warmed = lo1 == 0;   // h carries the true state
+    if (!warmed && a.warmup_tiles > 0)
+        warmed = lat ? warm_up<IO, CPL, ACC, HAS_Z, SP, true>(rg, m, a, ln, lo1, a.warmup_tiles, h)
+                     : warm_up<IO, CPL, ACC, HAS_Z, SP, false>(rg, m, a, ln, lo1, a.warmup_tiles, h);
     scan_piece_any<IO, CPL, ACC, HAS_Z, SP>(lat, rg, m, a, ln, lo1, hi1, h, dsum);
     const long long ord1 = wi - owner_of(static_cast<long long>(c1) * a.ntt, a.F, a.W);
     const bool withhold = single && ord1 == a.withheld;
-    if (lo1 == 0) {
+    if (warmed) {
         if (hi1 == a.ntt) {
             write_h_final<CPL>(a, ln, h);
-        } else if (single) {
+        } else if (single && !withhold) {
             write_rows<CPL>(incl_row<CPL>, a, wi, 0, h);
             publish(a, wi, kFlagInclusive);
         }
@@ -847,7 +1006,7 @@ __global__ void __launch_bounds__(kWpb * 32, SelCfg<IO, CPL>::MINB)
         f += hi;
     }
 
-    if (lo1 > 0) {
+    if (!warmed) {
         // carry-in of the first piece, its true final state, the correction
         float2 A2[CPL][8], carry[CPL][8];
         load_A2<CPL>(a.A_log, ln, A2);
@@ -978,6 +1137,7 @@ int launch_t(const void *x, const void *dt, const void *z, const void *Bm, const
     a.incl = reinterpret_cast<float *>(ws + lay.incl);
     a.st = call_status(workspace);
     a.withheld = g_withheld_split;
+    a.warmup_tiles = static_cast<int>(g_selective_warmup_steps / kT);
     a.timeout_ns = g_withheld_split >= 1 ? uint64_t(g_withheld_timeout_ms) * 1000000ull : kDefaultTimeoutNs;
     const bool hz = z != nullptr, sp = dt_softplus != 0;
     if (hz && sp) return launch_v<IO, ACC, true, true>(mp, a, p, stream);

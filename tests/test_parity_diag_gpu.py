@@ -33,13 +33,18 @@ def lr():
     return binding
 
 
+WARMUP_DEFAULT = 2048
+
+
 @pytest.fixture(autouse=True)
 def _clean_knobs(lr):
     lr.lr_set_split_override(0)
     lr.lr_test_withhold_split(-1, 1000)
+    lr.lr_set_selective_warmup(WARMUP_DEFAULT)
     yield
     lr.lr_set_split_override(0)
     lr.lr_test_withhold_split(-1, 1000)
+    lr.lr_set_selective_warmup(WARMUP_DEFAULT)
     assert lr.status() == 0
 
 
@@ -181,11 +186,32 @@ def test_selective_optional_inputs(lr, variant):
     check_sel(lr, p, "f32", **over)
 
 
+@pytest.mark.parametrize("warmup", [WARMUP_DEFAULT, 0])
 @pytest.mark.parametrize("splits", [2, 3, 5])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_selective_forced_time_splits_lookback(lr, splits, io):
+def test_selective_forced_time_splits(lr, splits, io, warmup):
+    """Pieces that start inside a sequence.  With the warm-up (default) each
+    rebuilds its state over the preceding steps -- here all the way from the
+    sequence start, since the slowest channels' horizon is longer than the
+    sequence; with it disabled the carry comes by decoupled look-back and the
+    outputs are corrected."""
     p = wl.selective_inputs(2, 650, 64, seed=20 + splits, io=io, with_h0=True)
     lr.lr_set_split_override(splits)
+    lr.lr_set_selective_warmup(warmup)
+    check_sel(lr, p, io)
+
+
+@pytest.mark.parametrize("warmup", [WARMUP_DEFAULT, 0])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_selective_warmup_stops_at_its_horizon(lr, io, warmup):
+    """Pieces of 1500 steps over the four decay scales of a 64-channel
+    chain: the warm-up windows end where the carry's contribution has decayed
+    below the cut-off (a few hundred to about 1200 steps back), inside the
+    preceding pieces, and the result still matches the oracle; the look-back
+    path on the same input for comparison."""
+    p = wl.selective_inputs(1, 6000, 64, seed=31, io=io, with_h0=True)
+    lr.lr_set_split_override(4)
+    lr.lr_set_selective_warmup(warmup)
     check_sel(lr, p, io)
 
 
@@ -316,6 +342,7 @@ def test_bounded_lookback_wait_reports_timeout_and_recovers(lr):
     after ~50 ms, the kernel finishes, and the status says LR_ERR_TIMEOUT."""
     p = wl.rglru_inputs(1, 512, 64, seed=3, io="f32", with_h0=True)
     lr.lr_set_split_override(4)
+    lr.lr_set_selective_warmup(0)   # selective pieces below take their carry by look-back
     lr.lr_test_withhold_split(1, 50)
     run_rglru(lr, p)
     assert lr.status() == lr.LR_ERR_TIMEOUT
