@@ -32,15 +32,22 @@
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  Argument errors are returned synchronously and launch
  *    nothing.  A failed launch returns LR_ERR_CUDA.
- *  - Errors detected on the device (a bounded wait that ran out) set a
- *    device-wide sticky status; lr_check_status() reads and clears it.
+ *  - Errors detected on the device (a bounded wait that ran out, an HGRN2
+ *    gate that is not a number) are recorded per call: the first 256 bytes
+ *    of the call's workspace hold its status word, stamped with the call, so
+ *    the word always describes the latest call that used the workspace.
+ *    lr_check_status(workspace, stream) reads and resets it.
  *  - State and arithmetic are float32 whatever the I/O dtype; bf16 outputs
  *    are rounded once, at the store.  There is no CPU fallback.
  *  - `workspace` is caller-owned device scratch of at least the size the
  *    matching *_workspace_size() call returns for the same sizes on the
- *    current device (0 bytes is possible; then workspace may be NULL).  Its
- *    contents need no initialisation.  Calls that overlap in time must use
- *    distinct workspaces.
+ *    current device: always at least 256 bytes (the status), also for an
+ *    empty problem; 0 means the arguments are invalid.  Its contents need no
+ *    initialisation.  Calls that overlap in time must use distinct
+ *    workspaces.
+ *  - The setters under "Tuning and test hooks" change process-wide settings
+ *    read at each call's launch; they are not synchronised with calls
+ *    running on other host threads.
  */
 #ifndef LRSCAN_H
 #define LRSCAN_H
@@ -68,7 +75,7 @@ enum {
     LR_ERR_WORKSPACE = -4,    /* workspace NULL or smaller than required */
     LR_ERR_CUDA = -5,         /* a CUDA runtime/driver call failed */
     LR_ERR_TIMEOUT = -6,      /* device side: a bounded wait ran out */
-    LR_ERR_RANGE = -7         /* device side: HGRN2 chunk log-gate spread too wide */
+    LR_ERR_RANGE = -7         /* device side: an HGRN2 gate that is not a finite number */
 };
 
 /* Human-readable name of a status code (static storage). */
@@ -219,7 +226,7 @@ int lr_rglru_scan_fwd_noalloc(const void *x, const void *r, const void *i,
  *   o_t = S_t q_t                              (after the update at t)
  *
  * and S_final[b,h] = S after the last step.  g is the forget gate after its
- * activation and lower bound, in (0, 1].
+ * activation and lower bound, in [0, 1].
  *
  * Layouts: q, k: (B, L, H*dk); v, g, o: (B, L, H*dv), all in `io`;
  *          S0, S_final: (B, H, dv, dk) fp32.  Optional: S0, S_final.
@@ -229,11 +236,21 @@ int lr_rglru_scan_fwd_noalloc(const void *x, const void *r, const void *i,
  *          chunked tcgen05 tensor-core kernel; every other shape or fp32 I/O
  *          runs a step-by-step CUDA-core kernel (fp32 arithmetic throughout,
  *          O(L dk dv) work, no gate-range limit; `chunk` is not used there).
- *          On the tensor-core path the product of a channel's gates within
- *          every chunk of 64 steps must stay above 2^-160 (always true when
- *          g >= 0.18, e.g. with a lower bound of 0.2); otherwise the kernel
- *          sets LR_ERR_RANGE and that chunk's outputs are not meaningful.
- * No workspace is needed (lr_hgrn2_workspace_size returns 0).
+ *          On the tensor-core path every gate in [0, 1] is handled: a
+ *          chunk whose gates decay too steeply for its factorisation is run in
+ *          shorter pieces, and a gate below 2^-120 (0 included) acts as a
+ *          reset of that state row.  The call is two launches: the first runs
+ *          every chunk whole and marks the thread blocks (64 value channels
+ *          of one batch row and head) that met a steep chunk; the second
+ *          re-runs only those, in pieces (it returns at once when none was
+ *          marked, and is not launched by lr_hgrn2_preact_fwd when
+ *          lb >= 0.18, which rules steep chunks out).  A gate that is not a finite number sets
+ *          LR_ERR_RANGE (read with lr_check_status); that call's outputs are
+ *          then not meaningful.  Gates above 1 lie outside the recurrence's
+ *          domain and give undefined results.
+ * Workspace: lr_hgrn2_workspace_size bytes: the call's device status and,
+ *          on the tensor-core path, one 8-byte mark per thread block
+ *          (B * H * 2).
  */
 size_t lr_hgrn2_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk,
                                int64_t dv, lr_dtype io);

@@ -178,7 +178,7 @@ const char *lr_status_string(int code) {
         case LR_ERR_WORKSPACE: return "LR_ERR_WORKSPACE: workspace missing or too small";
         case LR_ERR_CUDA: return "LR_ERR_CUDA: a CUDA call failed";
         case LR_ERR_TIMEOUT: return "LR_ERR_TIMEOUT: a bounded device-side wait ran out";
-        case LR_ERR_RANGE: return "LR_ERR_RANGE: HGRN2 chunk log-gate spread too wide";
+        case LR_ERR_RANGE: return "LR_ERR_RANGE: an HGRN2 gate is not a finite number";
         default: return "unknown lrscan status";
     }
 }
@@ -305,6 +305,7 @@ size_t lr_hgrn2_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk, int6
     (void)io;
     size_t bytes = 0;
     if (B < 0 || L < 0 || H <= 0) return 0;
+    if (B == 0 || L == 0) return lr::kStatusBytes;   // nothing launched: the status only
     if (lr::hgrn2_workspace(B, L, H, &bytes) != LR_OK) return SIZE_MAX;
     return bytes;
 }

@@ -17,6 +17,17 @@
 //   O    = 2^(Lambda - m) (.) ( tril(Q K^T) V~  +  2^m (.) Q S^T )
 //   dS^T = K^T V~'                                  (state update: S' = 2^Lambda_C (.) S + dS)
 //
+// Both factors stay within 2^(+-spread/2), where the spread is the sum of
+// |log2 g| over the range.  A chunk whose spread exceeds 160 for some
+// channel (small gates: the page's lower bound may be 0) is run as 2, 4, ..
+// "virtual chunks" of 32, 16, .. steps -- the smallest split whose pieces all
+// stay within 160 -- each one a pass through the same pipeline with the
+// steps outside it masked out; the terms between virtual chunks then flow
+// through the state, whose factors never exceed 1.  Log-gates are clamped at
+// -120 per step (a gate below 2^-120, e.g. 0, resets the state to within
+// fp32 resolution), so a single step always fits.  Non-finite gates set
+// LR_ERR_RANGE.
+//
 // A thread block owns 64 value rows of one (batch, head) (rows of S evolve
 // independently because diag(g) scales rows): grid = B * H * 2, one block per
 // SM (218 KB of shared memory, all 512 TMEM columns).  Four tcgen05 MMAs per
@@ -63,9 +74,11 @@ constexpr int FSTEPS = 64 / FQ;    // steps per front thread
 constexpr int TMA_WARP = KW + FW, MMA_WARP = KW + FW + 1, OX_WARP = KW + FW + 2;
 constexpr int THREADS = 32 * (KW + FW + 3);
 constexpr int NST = 3;         // TMA stages
-// largest per-chunk spread of Lambda (log2 units) the reference split keeps
-// inside fp32 range with headroom: 2^(+-80) factors
+// largest spread of Lambda (log2 units) over a virtual chunk that the
+// reference split keeps inside fp32 range with headroom: 2^(+-80) factors
 constexpr float kMaxSpread = 160.0f;
+// per-step floor of log2 g: one step always fits a virtual chunk
+constexpr float kMinLog2 = -120.0f;
 
 // stage: Q [64 t][128 j] and K [64 s][128 j] as two 128B-swizzled 64-column
 // halves each; V and g [64 t][64 i] as plain bf16 rows
@@ -81,10 +94,15 @@ constexpr uint32_t OFF_E1 = OFF_SBT + 16384;       // 2 x 2^(Lambda - m), fp32 [
 constexpr uint32_t OFF_EM = OFF_E1 + 2 * 16384;    // 2 x 2^m [64]
 constexpr uint32_t OFF_GC = OFF_EM + 2 * 256;      // 2 x 2^Lambda_C [64]
 constexpr uint32_t OFF_TOT = OFF_GC + 2 * 256;     // front: per-quarter totals [FQ][64]
-constexpr uint32_t OFF_L0 = OFF_TOT + FQ * 256;    // front: Lambda_0 [64]
-constexpr uint32_t OFF_BAR = OFF_L0 + 256;
-// full[3] empty[3] bar_p[2] bar_o[2] bar_x[2] fdone[2] kdone[2] sbready mma_done
-constexpr int NBAR = 3 + 3 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+constexpr uint32_t OFF_VI = OFF_TOT + FQ * 256;    // 2 x virtual chunk (chunk, lo, hi, last)
+constexpr uint32_t OFF_SPL = OFF_VI + 32;          // front: split flags of the chunk; [4..7]
+                                                   // virtual chunks of chunk c % 4
+constexpr uint32_t OFF_BAR = OFF_SPL + 32;
+// full[3] empty[3] bar_p[2] bar_o[2] bar_x[2] fdone[2] kdone[2] sbready mma_done splitr[2]
+constexpr int NBAR = 3 + 3 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 2;
+// the local test that rules out a split: every quarter (16 steps) of every
+// row within a quarter of the limit
+constexpr float kQuarterSafe = kMaxSpread / 4;
 constexpr uint32_t OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr uint32_t OFF_FLAG = OFF_TMEM + 8;
 constexpr uint32_t SMEM = OFF_FLAG + 8;
@@ -129,21 +147,264 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&p);
 }
+
+// Bounded mbarrier wait of the block's roles: the first wait to run out sets
+// the block's abort flag, so that every role leaves its loop instead of
+// waiting out its own limit.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              uint64_t timeout_ns, StatusRef sref) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag != 0) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            status_report(sref, LR_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// What a front thread works with.
+struct FrontEnv {
+    unsigned char *sm;
+    uint32_t tmem;
+    uint64_t *empty, *bar_p, *bar_o, *fdone, *kdone, *splitr;
+    volatile int *abort_flag;
+    volatile int *VI;          // [2][chunk, lo, hi, last]
+    volatile unsigned *NVC;    // [4] virtual chunks of chunk c % 4
+    int L;
+    float lb;
+    uint64_t timeout_ns;
+    StatusRef sref;
+};
+
+// One virtual chunk [lo, hi) of chunk c by the front: V~, V~', the masked P,
+// 2^(Lambda - m), 2^(m - B0) and the decay 2^(B1 - B0), then the hand-over to
+// the MMA issuer and the back.  loc: this thread's cumulative log2 gates
+// (from the chunk start); B0, B1: Lambda before the virtual chunk and at its
+// last step.  WHOLE: the chunk is not split (lo = 0, hi = 64), so no step is
+// masked.  Returns false when a wait failed (every front thread then returns
+// false).
+template <bool SPLIT, bool WHOLE>
+__device__ __forceinline__ bool front_vc(const FrontEnv &x, int c, int j, int nvc, int lo, int hi,
+                                         const float (&loc)[FSTEPS], float B0, float B1, int &v) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int f = tid - 32 * KW, fw = warp - KW;
+    const int i = f & (RB - 1), qt = f / RB;
+    const int tb = FSTEPS * qt;
+    const int st = c % NST, bi = v & 1;
+    const unsigned char *stg = x.sm + st * STAGE_BYTES;
+    const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(stg + OFF_V);
+    float *E1 = reinterpret_cast<float *>(x.sm + OFF_E1);
+    float *EM = reinterpret_cast<float *>(x.sm + OFF_EM);
+    float *GC = reinterpret_cast<float *>(x.sm + OFF_GC);
+    unsigned char *Ps = x.sm + OFF_PS, *VT = x.sm + OFF_VT, *VTP = x.sm + OFF_VTP;
+    // 2^(Lambda - m) buffer free (back done with virtual chunk v-2)
+    bool ok = v < 2 || wait_or_abort(&x.kdone[bi], ((v - 2) >> 1) & 1, x.abort_flag, x.timeout_ns, x.sref);
+    // m = the mean of B0 and B1 keeps every factor within 2^(+-spread/2)
+    const float m = 0.5f * (B0 + B1);
+    float *e1 = E1 + bi * (C * RB);
+#pragma unroll
+    for (int u = 0; u < FSTEPS; ++u) {
+        const int t = tb + u;
+        e1[e1_index(t, i)] = (WHOLE || (t >= lo && t < hi)) ? ex2_approx(loc[u] - m) : 0.0f;
+    }
+    if (WHOLE ? qt == 0 : qt == lo / FSTEPS) {
+        EM[bi * RB + i] = ex2_approx(m - B0);
+        GC[bi * RB + i] = ex2_approx(B1 - B0);
+    }
+    // V~ = 2^(m - Lambda) v and V~' = 2^(B1 - m) V~ for row i, this thread's
+    // steps inside the virtual chunk
+    const float cm = ex2_approx(B1 - m);
+    uint32_t vt[FSTEPS / 2], vtp[FSTEPS / 2];
+#pragma unroll
+    for (int u = 0; u < FSTEPS; u += 2) {
+        const int t = tb + u;
+        const float w0 = (WHOLE || (t >= lo && t < hi)) ? ex2_approx(m - loc[u]) * __bfloat162float(sV[t * RB + i])
+                                                        : 0.0f;
+        const float w1 = (WHOLE || (t + 1 >= lo && t + 1 < hi))
+                             ? ex2_approx(m - loc[u + 1]) * __bfloat162float(sV[(t + 1) * RB + i])
+                             : 0.0f;
+        vt[u / 2] = pack_bf16(w0, w1);
+        vtp[u / 2] = pack_bf16(w0 * cm, w1 * cm);
+    }
+    // the V~, V~' and masked-P buffers are free once dS and OI of virtual
+    // chunk v-1 completed (the work above overlapped with them); P_c is ready
+    if (ok && v >= 1)
+        ok = wait_or_abort(&x.bar_o[(v - 1) & 1], ((v - 1) >> 1) & 1, x.abort_flag, x.timeout_ns, x.sref);
+    if (ok) ok = wait_or_abort(&x.bar_p[c & 1], (c >> 1) & 1, x.abort_flag, x.timeout_ns, x.sref);
+    ok = __all_sync(0xffffffffu, ok);   // the TMEM load below is warp-collective
+    if (ok) {
+#pragma unroll
+        for (int k = 0; k < FSTEPS / 8; ++k) {
+            const uint32_t o8 = sw128_offset(i, tb + 8 * k);
+            *reinterpret_cast<uint4 *>(VT + o8) = make_uint4(vt[4 * k], vt[4 * k + 1], vt[4 * k + 2], vt[4 * k + 3]);
+            *reinterpret_cast<uint4 *>(VTP + o8) =
+                make_uint4(vtp[4 * k], vtp[4 * k + 1], vtp[4 * k + 2], vtp[4 * k + 3]);
+        }
+        // causal mask of P_c inside the virtual chunk: the M = 64 rows t sit in
+        // lanes 0..15 of each warp quarter; the two warps of a quarter take 32
+        // columns s each, their half-warps 16 columns each (two-half TMEM load)
+        tc_fence_after();
+        const int quarter = fw & 3;
+        const int s_base = 32 * (fw >> 2) + 16 * (lane >> 4);
+        float pv[16];
+        tmem_ld16x2_nowait<16>(x.tmem + T_P + (c & 1) * 64 + 32 * (fw >> 2) + (uint32_t(quarter * 32) << 16), pv);
+        tmem_ld_wait_tied(pv);
+        const int t = 16 * quarter + (lane & 15);
+        const bool row_in = WHOLE || (t >= lo && t < hi);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int s0 = s_base + ch * 8 + 2 * e;
+                w4[e] = pack_bf16(row_in && s0 <= t && (WHOLE || s0 >= lo) ? pv[ch * 8 + 2 * e] : 0.0f,
+                                  row_in && s0 + 1 <= t && (WHOLE || s0 + 1 >= lo) ? pv[ch * 8 + 2 * e + 1] : 0.0f);
+            }
+            const int chunk = (s_base >> 3) + ch;
+            *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    if (named_bar_or(2, 32 * FW, !ok)) return false;
+    if (f == 0) {
+        const bool last = j == nvc - 1;
+        if (SPLIT) {
+            x.VI[4 * bi] = c;
+            x.VI[4 * bi + 1] = lo;
+            x.VI[4 * bi + 2] = hi;
+            x.VI[4 * bi + 3] = last ? 1 : 0;
+        }
+        arrive(&x.fdone[bi]);
+        if (last) arrive(&x.empty[st]);   // V, g of stage st no longer read
+    }
+    ++v;
+    return true;
+}
+
+// A chunk some quarter of which decays beyond kQuarterSafe: its log-gates
+// again with the per-step floor kMinLog2 (a gate of 0 gives -inf), the
+// finest split into virtual chunks of 64 >> lvl steps whose every piece
+// stays within kMaxSpread for every row, and the virtual chunks.
+template <bool PRE>
+__device__ __forceinline__ bool front_split_chunk(const FrontEnv &x, int c, int &v) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int f = tid - 32 * KW;
+    const int i = f & (RB - 1), qt = f / RB;
+    const int tb = FSTEPS * qt;
+    const int t0 = c * C;
+    const __nv_bfloat16 *sG = reinterpret_cast<const __nv_bfloat16 *>(x.sm + (c % NST) * STAGE_BYTES + OFF_G);
+    float *TOTF = reinterpret_cast<float *>(x.sm + OFF_TOT);
+    unsigned *SPL = reinterpret_cast<unsigned *>(x.sm + OFF_SPL);
+    float loc[FSTEPS];
+    float acc = 0.0f;
+#pragma unroll
+    for (int u = 0; u < FSTEPS; ++u) {
+        const int t = tb + u;
+        float gv = __bfloat162float(sG[t * RB + i]);
+        if (PRE) gv = fmaf(1.0f - x.lb, rcp_approx(1.0f + ex2_approx(-gv * kLog2e)), x.lb);
+        acc += t0 + t < x.L ? fmaxf(lg2_approx(gv), kMinLog2) : 0.0f;
+        loc[u] = acc;
+    }
+    // bit k of `need` set = some aligned run of 64 >> k steps of some row
+    // sums to more than kMaxSpread in |log2 g|
+    unsigned need = 0;
+    if (-acc > kMaxSpread) {   // runs inside this quarter (16 .. 1 steps)
+        need |= 4u;
+#pragma unroll 1
+        for (int k = 3; k <= 6; ++k) {
+            const int len = 64 >> k;
+#pragma unroll 1
+            for (int a0 = 0; a0 < FSTEPS; a0 += len) {
+                float before = 0.0f, end = 0.0f;
+#pragma unroll
+                for (int u = 0; u < FSTEPS; ++u) {
+                    if (u == a0 - 1) before = loc[u];
+                    if (u == a0 + len - 1) end = loc[u];
+                }
+                if (before - end > kMaxSpread) need |= 1u << k;
+            }
+        }
+    }
+    named_bar(3, 32 * FW);   // every thread is past its reads of the previous totals
+    TOTF[qt * RB + i] = acc;
+    if (f == 0) SPL[0] = 0;
+    named_bar(3, 32 * FW);
+    float off = 0.0f, cq[FQ + 1];
+    cq[0] = 0.0f;
+#pragma unroll
+    for (int q = 0; q < FQ; ++q) {
+        const float tq = TOTF[q * RB + i];
+        off += q < qt ? tq : 0.0f;
+        cq[q + 1] = cq[q] + tq;   // cumulative Lambda at the end of quarter q
+    }
+    if (qt == 0) {
+        if (-cq[FQ] > kMaxSpread) need |= 1u;
+        if (-cq[2] > kMaxSpread || cq[2] - cq[FQ] > kMaxSpread) need |= 2u;
+    }
+    need = __reduce_or_sync(0xffffffffu, need);
+    if (lane == 0 && need != 0) atomicOr(SPL, need);
+    named_bar(3, 32 * FW);
+    need = SPL[0];
+    int lvl = 0;
+    while (lvl < 6 && ((need >> lvl) & 1u)) ++lvl;
+#pragma unroll
+    for (int u = 0; u < FSTEPS; ++u) loc[u] += off;
+    const int len = C >> lvl, nvc = 1 << lvl;
+    if (f == 0) {   // tell the OX issuer
+        x.NVC[c & 3] = nvc;
+        arrive(&x.splitr[c & 1]);
+    }
+    for (int j = 0; j < nvc; ++j) {
+        const int lo = j * len, hi = lo + len;
+        float B0 = 0.0f, B1 = 0.0f;
+        if (len >= FSTEPS) {
+            B0 = cq[lo / FSTEPS];
+            B1 = cq[hi / FSTEPS];
+        } else if (qt == lo / FSTEPS) {   // inside this row's quarter
+            B0 = lo == tb ? off : 0.0f;
+#pragma unroll
+            for (int u = 0; u < FSTEPS; ++u) {
+                if (tb + u == lo - 1) B0 = loc[u];
+                if (tb + u == hi - 1) B1 = loc[u];
+            }
+        }
+        if (!front_vc<true, false>(x, c, j, nvc, lo, hi, loc, B0, B1, v)) return false;
+    }
+    return true;
+}
 }  // namespace hg
 
 // PRE: the gate arrives as the pre-activation f and the front forms
 // g = lb + (1 - lb) sigmoid(f) ([HGRN2] lower-bounded, sigmoid-activated gate).
-template <bool PRE>
+//
+// A call runs in two passes over the same grid.  SPLIT = false: every chunk
+// whole; a block that meets a chunk some quarter of which decays beyond
+// kQuarterSafe (a split may be needed) writes the call's stamp into its
+// redo word and carries on (its results are then discarded).  SPLIT = true:
+// only the blocks whose redo word holds the stamp run, from the start,
+// splitting chunks into virtual chunks where needed; the others return at
+// once.  So the common case runs code without the split path's registers
+// and branches.
+template <bool PRE, bool SPLIT>
 __global__ void __launch_bounds__(hg::THREADS, 1)
     hgrn2_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                        const float *__restrict__ S0, float *__restrict__ S_final,
                        __nv_bfloat16 *__restrict__ o, int L, int H, int n_chunks, float lb,
-                       uint64_t timeout_ns, StatusRef sref) {
+                       uint64_t timeout_ns, StatusRef sref, unsigned long long *__restrict__ redo) {
     using namespace hg;
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (tid == 0 && blockIdx.x == 0) status_begin(sref);
+    if (SPLIT) {
+        if (redo[blockIdx.x] != sref.stamp) return;   // the first pass was right
+    } else if (tid == 0 && blockIdx.x == 0) {
+        status_begin(sref);
+    }
     if ((smem_u32(sm) & 1023u) != 0) {  // swizzled tiles need a 1024-byte aligned base
         if (tid == 0) status_report(sref, LR_ERR_CUDA);
         return;
@@ -157,13 +418,15 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *full = bars, *empty = bars + 3, *bar_p = bars + 6, *bar_o = bars + 8,
              *bar_x = bars + 10, *fdone = bars + 12, *kdone = bars + 14, *sbready = bars + 16,
-             *mma_done = bars + 17;
+             *mma_done = bars + 17, *splitr = bars + 18;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_FLAG);
     float *E1 = reinterpret_cast<float *>(sm + OFF_E1);
     float *EM = reinterpret_cast<float *>(sm + OFF_EM);
     float *GC = reinterpret_cast<float *>(sm + OFF_GC);
     unsigned char *Ps = sm + OFF_PS, *VT = sm + OFF_VT, *VTP = sm + OFF_VTP, *SBT = sm + OFF_SBT;
+    volatile int *VI = reinterpret_cast<volatile int *>(sm + OFF_VI);   // [2][chunk, lo, hi, last]
+    volatile unsigned *NVC = reinterpret_cast<volatile unsigned *>(sm + OFF_SPL) + 4;   // [4]
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -179,6 +442,8 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
         }
         mbar_init(sbready, KW);   // each back warp publishes its own 32 rows
         mbar_init(mma_done, 2);
+        mbar_init(&splitr[0], 1);
+        mbar_init(&splitr[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -188,20 +453,8 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // Bounded wait; the first wait to run out sets the block's abort flag so
-    // that every role leaves its loop instead of waiting out its own limit.
     auto hw = [&](uint64_t *bar, uint32_t parity) -> bool {
-        if (mbar_try_wait(bar, parity)) return true;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar, parity)) {
-            if (*abort_flag != 0) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) {
-                *abort_flag = 1;
-                status_report(sref, LR_ERR_TIMEOUT);
-                return false;
-            }
-        }
-        return true;
+        return hg::wait_or_abort(bar, parity, abort_flag, timeout_ns, sref);
     };
 
     if (warp == TMA_WARP) {  // ------------------------------------------- TMA
@@ -244,21 +497,22 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                 tc_fence_after();
                 issue_p(0);
             }
-            for (int c = 0; ok && c < n_chunks; ++c) {
-                const int st = c % NST, bi = c & 1;
-                const uint32_t sQ = smem_u32(sm + st * STAGE_BYTES), sK = sQ + OFF_K;
-                // P of the next chunk: its buffer held P_{c-1}, masked once the
-                // front finished chunk c-1
-                if (c + 1 < n_chunks) {
+            bool first = true;   // virtual chunk v starts chunk c
+            for (int c = 0, v = 0; ok && c < n_chunks; ++v) {
+                const int st = c % NST, bi = v & 1;
+                const uint32_t sK = smem_u32(sm + st * STAGE_BYTES) + OFF_K;
+                // P of the next chunk: its buffer held P_{c-1}, which the front
+                // masked for the last time in virtual chunk v-1
+                if (first && c + 1 < n_chunks) {
                     if (!hw(&full[(c + 1) % NST], ((c + 1) / NST) & 1)) break;
-                    if (c >= 1 && !hw(&fdone[(c - 1) & 1], ((c - 1) >> 1) & 1)) break;
                     tc_fence_after();
                     issue_p(c + 1);
                 }
-                // dS_c and OI_c once the front wrote V~', V~ and the masked P of
-                // chunk c and the back released the accumulators of chunk c-2
-                if (!hw(&fdone[bi], (c >> 1) & 1)) break;
-                if (c >= 2 && !hw(&kdone[bi], ((c - 2) >> 1) & 1)) break;
+                // dS_v and OI_v once the front wrote V~', V~ and the masked P of
+                // virtual chunk v and the back released the accumulators of v-2
+                if (!hw(&fdone[bi], (v >> 1) & 1)) break;
+                const bool last = !SPLIT || VI[4 * bi + 3] != 0;
+                if (v >= 2 && !hw(&kdone[bi], ((v - 2) >> 1) & 1)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C / 16; ++kk)
@@ -269,7 +523,11 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                     umma_bf16(tmem + T_OI + bi * 64, umma_smem_desc(smem_u32(Ps) + kk * 32, 16, 1024),
                               umma_smem_desc(smem_u32(VT) + kk * 32, 16, 1024), IDESC_OI, kk > 0);
                 umma_commit(&bar_o[bi]);
-                umma_commit(&empty[st]);   // K_c no longer read once these complete
+                if (last) {
+                    umma_commit(&empty[st]);   // K_c no longer read once these complete
+                    ++c;
+                }
+                first = last;
             }
             // nothing of this block's may still run on the tensor cores when
             // its TMEM is released
@@ -278,13 +536,22 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
         }
     } else if (warp == OX_WARP) {  // -------------------------------------- OX
         if (lane == 0) {
-            for (int c = 0; c < n_chunks; ++c) {
-                const int st = c % NST, bi = c & 1;
-                // the bf16 state after chunk c-1, Q_c, and the OX buffer of
-                // chunk c-2 released by the back
-                if (!hw(sbready, c & 1)) break;
+            unsigned nvc = 0, j = 0;   // virtual chunks of chunk c, this one's index
+            for (int c = 0, v = 0; c < n_chunks; ++v) {
+                const int st = c % NST, bi = v & 1;
+                // the bf16 state after virtual chunk v-1, how many virtual
+                // chunks chunk c has (the front publishes it as soon as it has
+                // decided), Q_c, and the OX buffer of v-2 released by the back
+                if (!hw(sbready, v & 1)) break;
+                if (!SPLIT) {
+                    nvc = 1;
+                } else if (j == 0) {
+                    if (!hw(&splitr[c & 1], (c >> 1) & 1)) break;
+                    nvc = NVC[c & 3];
+                }
+                const bool last = ++j == nvc;
                 if (!hw(&full[st], (c / NST) & 1)) break;
-                if (c >= 2 && !hw(&kdone[bi], ((c - 2) >> 1) & 1)) break;
+                if (v >= 2 && !hw(&kdone[bi], ((v - 2) >> 1) & 1)) break;
                 tc_fence_after();
                 const uint32_t sQ = smem_u32(sm + st * STAGE_BYTES);
 #pragma unroll
@@ -294,25 +561,27 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                               umma_smem_desc(smem_u32(SBT) + kk * 2048, 8192, 1024), IDESC_OX, kk > 0);
                 }
                 umma_commit(&bar_x[bi]);
-                umma_commit(&empty[st]);   // Q_c no longer read once these complete
+                if (last) {
+                    umma_commit(&empty[st]);   // Q_c no longer read once these complete
+                    j = 0;
+                    ++c;
+                }
             }
             umma_commit(mma_done);
             mbar_wait_bounded(mma_done, 0, timeout_ns);
         }
     } else if (warp >= KW) {  // ----------------------------------------- front
-        const int f = tid - 32 * KW, fw = warp - KW;
+        const int f = tid - 32 * KW;
         const int i = f & (RB - 1), qt = f / RB;   // value row, quarter of the chunk's steps
         const int tb = FSTEPS * qt;
         float *TOTF = reinterpret_cast<float *>(sm + OFF_TOT);
-        float *L0F = reinterpret_cast<float *>(sm + OFF_L0);
+        const hg::FrontEnv fx{sm, tmem, empty, bar_p, bar_o, fdone, kdone, splitr, abort_flag, VI, NVC,
+                              L, lb, timeout_ns, sref};
+        int v = 0;   // virtual chunks so far
         for (int c = 0; c < n_chunks; ++c) {
-            const int st = c % NST, bi = c & 1;
-            const unsigned char *stg = sm + st * STAGE_BYTES;
-            const __nv_bfloat16 *sV = reinterpret_cast<const __nv_bfloat16 *>(stg + OFF_V);
-            const __nv_bfloat16 *sG = reinterpret_cast<const __nv_bfloat16 *>(stg + OFF_G);
-            // inputs landed; 2^(Lambda - m) buffer free (back done with chunk c-2)
-            bool ok = hw(&full[st], (c / NST) & 1);
-            if (ok && c >= 2) ok = hw(&kdone[bi], ((c - 2) >> 1) & 1);
+            const int st = c % NST;
+            const __nv_bfloat16 *sG = reinterpret_cast<const __nv_bfloat16 *>(sm + st * STAGE_BYTES + OFF_G);
+            const bool ok = hw(&full[st], (c / NST) & 1);   // inputs landed
 
             // cumulative log2 gates over this thread's steps (steps past L: g = 1)
             const int t0 = c * C;
@@ -326,11 +595,22 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                 acc += t0 + t < L ? lg2_approx(gv) : 0.0f;
                 loc[u] = acc;
             }
+            // a gate that is not a number (or infinite) leaves NaN or +inf here
+            if (!(acc == acc) || acc == __int_as_float(0x7f800000)) status_report(sref, LR_ERR_RANGE);
             TOTF[qt * RB + i] = acc;
-            if (qt == 0) L0F[i] = loc[0];
-            // the quarter totals are exchanged here; a failed wait anywhere ends
-            // the loop for every front thread together
-            if (named_bar_or(2, 32 * FW, !ok)) break;
+            // the quarter totals are exchanged here.  The barrier also ORs the
+            // local test that rules out a split (this quarter's |sum of log2 g|
+            // within kQuarterSafe) with a failed wait; only when it fires do
+            // the front threads tell the two apart and, rarely, split the chunk
+            if (named_bar_or(2, 32 * FW, !ok || -acc > kQuarterSafe)) {
+                if (named_bar_or(3, 32 * FW, !ok)) break;
+                if constexpr (SPLIT) {
+                    if (!hg::front_split_chunk<PRE>(fx, c, v)) break;
+                    continue;
+                } else {
+                    if (f == 0) redo[blockIdx.x] = sref.stamp;   // the second pass redoes this block
+                }
+            }
             float off = 0.0f, lc = 0.0f;
 #pragma unroll
             for (int q = 0; q < FQ; ++q) {
@@ -340,73 +620,11 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             }
 #pragma unroll
             for (int u = 0; u < FSTEPS; ++u) loc[u] += off;
-            const float l0 = L0F[i];
-            const float m = 0.5f * (l0 + lc);
-            if (qt == 0 && !(l0 - lc <= kMaxSpread)) status_report(sref, LR_ERR_RANGE);
-            float *e1 = E1 + bi * (C * RB);
-#pragma unroll
-            for (int u = 0; u < FSTEPS; ++u) e1[e1_index(tb + u, i)] = ex2_approx(loc[u] - m);
-            if (qt == 0) {
-                EM[bi * RB + i] = ex2_approx(m);
-                GC[bi * RB + i] = ex2_approx(lc);
+            if (SPLIT && f == 0) {   // one virtual chunk: tell the OX issuer
+                NVC[c & 3] = 1;
+                arrive(&splitr[c & 1]);
             }
-            // V~ = 2^(m - Lambda) v and V~' = 2^(Lambda_C - m) V~ for row i, these steps
-            const float cm = ex2_approx(lc - m);
-            uint32_t vt[FSTEPS / 2], vtp[FSTEPS / 2];
-#pragma unroll
-            for (int u = 0; u < FSTEPS; u += 2) {
-                const int t = tb + u;
-                const float w0 = ex2_approx(m - loc[u]) * __bfloat162float(sV[t * RB + i]);
-                const float w1 = ex2_approx(m - loc[u + 1]) * __bfloat162float(sV[(t + 1) * RB + i]);
-                vt[u / 2] = pack_bf16(w0, w1);
-                vtp[u / 2] = pack_bf16(w0 * cm, w1 * cm);
-            }
-            // the V~, V~' and masked-P buffers are free once dS and OI of chunk
-            // c-1 completed (the work above overlapped with them); P_c is ready
-            ok = c == 0 || hw(&bar_o[(c - 1) & 1], ((c - 1) >> 1) & 1);
-            if (ok) ok = hw(&bar_p[bi], (c >> 1) & 1);
-            ok = __all_sync(0xffffffffu, ok);   // the TMEM load below is warp-collective
-            if (ok) {
-#pragma unroll
-                for (int k = 0; k < FSTEPS / 8; ++k) {
-                    const uint32_t o8 = sw128_offset(i, tb + 8 * k);
-                    *reinterpret_cast<uint4 *>(VT + o8) =
-                        make_uint4(vt[4 * k], vt[4 * k + 1], vt[4 * k + 2], vt[4 * k + 3]);
-                    *reinterpret_cast<uint4 *>(VTP + o8) =
-                        make_uint4(vtp[4 * k], vtp[4 * k + 1], vtp[4 * k + 2], vtp[4 * k + 3]);
-                }
-                // causal mask of P_c: the M = 64 rows t sit in lanes 0..15 of each
-                // warp quarter; the two warps of a quarter take 32 columns s each,
-                // their half-warps 16 columns each (two-half TMEM load)
-                tc_fence_after();
-                const int quarter = fw & 3;
-                const int s_base = 32 * (fw >> 2) + 16 * (lane >> 4);
-                float pv[16];
-                tmem_ld16x2_nowait<16>(tmem + T_P + bi * 64 + 32 * (fw >> 2) +
-                                           (uint32_t(quarter * 32) << 16), pv);
-                tmem_ld_wait_tied(pv);
-                const int t = 16 * quarter + (lane & 15);
-#pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s0 = s_base + ch * 8 + 2 * e;
-                        w4[e] = pack_bf16(s0 <= t ? pv[ch * 8 + 2 * e] : 0.0f,
-                                          s0 + 1 <= t ? pv[ch * 8 + 2 * e + 1] : 0.0f);
-                    }
-                    const int chunk = (s_base >> 3) + ch;
-                    *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (named_bar_or(2, 32 * FW, !ok)) break;
-            if (f == 0) {
-                arrive(&fdone[bi]);
-                arrive(&empty[st]);   // V, g of stage st no longer read
-            }
+            if (!hg::front_vc<SPLIT, true>(fx, c, 0, 1, 0, C, loc, 0.0f, lc, v)) break;
         }
     } else {  // ------------------------------------------------------------ back
         // key column j = tid of value rows rb*64 .. rb*64+63 of S[b, h].  The
@@ -436,11 +654,13 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
         // lane % 16 at columns [16 hh, +16) and [32 + 16 hh, +16)
         const int t = 16 * warp + (lane & 15);
         const int cb = 32 * (lane >> 4);
-        for (int c = 0; c < n_chunks; ++c) {
-            const int bi = c & 1;
-            bool ok = hw(&fdone[bi], (c >> 1) & 1);
-            if (ok) ok = hw(&bar_o[bi], (c >> 1) & 1);
+        for (int c = 0, v = 0; c < n_chunks; ++v) {
+            const int bi = v & 1;
+            bool ok = hw(&fdone[bi], (v >> 1) & 1);
+            if (ok) ok = hw(&bar_o[bi], (v >> 1) & 1);
             if (!__all_sync(FULLM, ok)) break;
+            const int lo = SPLIT ? VI[4 * bi + 1] : 0, hi = SPLIT ? VI[4 * bi + 2] : C;
+            const bool last = !SPLIT || VI[4 * bi + 3] != 0;
             tc_fence_after();
             {   // S = diag(2^Lambda_C) S + dS   (dS^T lane j, column i)
                 const float *gc = GC + bi * RB;
@@ -466,8 +686,8 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                     }
                 }
             }
-            // OX_c reads the previous bf16 state until bar_x
-            ok = hw(&bar_x[bi], (c >> 1) & 1);
+            // OX_v reads the previous bf16 state until bar_x
+            ok = hw(&bar_x[bi], (v >> 1) & 1);
             if (!__all_sync(FULLM, ok)) break;
             tc_fence_after();
             // the first output columns' accumulator loads overlap the state write
@@ -477,7 +697,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             write_state();
             const float *e1 = E1 + bi * (C * RB);
             const float *em = EM + bi * RB;
-            const bool store = c * C + t < L;
+            const bool store = c * C + t < L && t >= lo && t < hi;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 if (hh > 0) {
@@ -507,6 +727,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive(&kdone[bi]);
+            if (last) ++c;
         }
         if (S_final != nullptr) {
 #pragma unroll
@@ -554,22 +775,32 @@ bool hg_map(CUtensorMap *tm, const void *base, uint64_t cols, uint64_t L, uint64
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <typename K>
+bool hg_smem_attr(K kern) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hg::SMEM)) ==
+           cudaSuccess;
+}
+
 bool hg_setup_once() {
     static std::once_flag once;
     static bool ok = false;
     std::call_once(once, [] {
-        ok = cudaFuncSetAttribute(hgrn2_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(hg::SMEM)) == cudaSuccess &&
-             cudaFuncSetAttribute(hgrn2_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(hg::SMEM)) == cudaSuccess;
+        ok = hg_smem_attr(hgrn2_chunk_kernel<false, false>) && hg_smem_attr(hgrn2_chunk_kernel<false, true>) &&
+             hg_smem_attr(hgrn2_chunk_kernel<true, false>) && hg_smem_attr(hgrn2_chunk_kernel<true, true>);
     });
     return ok;
 }
 
+// A lower-bounded gate g >= lb keeps every quarter of a chunk within
+// kQuarterSafe when 16 * -log2(lb) <= kQuarterSafe, i.e. lb >= 2^-2.5 =
+// 0.177; above 0.18 the second pass cannot have work and is not launched.
+constexpr float kLbNoSplit = 0.18f;
+
 }  // namespace
 
-int hgrn2_workspace(int64_t, int64_t, int64_t, size_t *bytes) {
-    *bytes = kStatusBytes;   // the call status only
+int hgrn2_workspace(int64_t B, int64_t, int64_t H, size_t *bytes) {
+    // the call status, then one redo word per thread block
+    *bytes = kStatusBytes + size_t(B) * size_t(H) * hg::NRB * sizeof(unsigned long long);
     return LR_OK;
 }
 
@@ -586,10 +817,18 @@ int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, con
     const int64_t grid = B * H * hg::NRB;
     const uint64_t timeout = g_withheld_split >= 1 ? uint64_t(g_withheld_timeout_ms) * 1000000ull
                                                    : kDefaultTimeoutNs;
-    auto kern = preact ? hgrn2_chunk_kernel<true> : hgrn2_chunk_kernel<false>;
-    kern<<<static_cast<unsigned>(grid), hg::THREADS, hg::SMEM, stream>>>(
+    const StatusRef sref = call_status(workspace);   // one stamp for both passes
+    auto *redo = reinterpret_cast<unsigned long long *>(static_cast<unsigned char *>(workspace) + kStatusBytes);
+    auto first = preact ? hgrn2_chunk_kernel<true, false> : hgrn2_chunk_kernel<false, false>;
+    first<<<static_cast<unsigned>(grid), hg::THREADS, hg::SMEM, stream>>>(
         mq, mk, mv, mg, S0, S_final, static_cast<__nv_bfloat16 *>(o), static_cast<int>(L),
-        static_cast<int>(H), n_chunks, lb, timeout, call_status(workspace));
+        static_cast<int>(H), n_chunks, lb, timeout, sref, redo);
+    if (cudaGetLastError() != cudaSuccess) return LR_ERR_CUDA;
+    if (preact && lb >= kLbNoSplit) return LR_OK;
+    auto second = preact ? hgrn2_chunk_kernel<true, true> : hgrn2_chunk_kernel<false, true>;
+    second<<<static_cast<unsigned>(grid), hg::THREADS, hg::SMEM, stream>>>(
+        mq, mk, mv, mg, S0, S_final, static_cast<__nv_bfloat16 *>(o), static_cast<int>(L),
+        static_cast<int>(H), n_chunks, lb, timeout, sref, redo);
     return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 

@@ -138,6 +138,8 @@ def test_workspace_size_of_empty_problems_is_the_call_status(lr):
     assert lr.lr_rglru_scan_workspace_size(1, 0, 64, 1) == 256
     assert lr.lr_minmax_scan_workspace_size(1, 4, 0, 1) == 256
     assert lr.lr_hgrn2_workspace_size(1, 0, 2, 128, 128, 1) == 256
+    # HGRN2 adds one 8-byte redo mark per thread block (B * H * 2 blocks)
+    assert lr.lr_hgrn2_workspace_size(2, 64, 3, 128, 128, 1) == 256 + 2 * 3 * 2 * 8
     assert lr.lr_hgrn2_workspace_size(1, 0, 0, 128, 128, 1) == 0         # H == 0
 
 

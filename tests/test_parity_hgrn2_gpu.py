@@ -79,12 +79,81 @@ def test_hgrn2_split_resume(lr):
     assert rel_err(S2.cpu(), Sf.cpu()) <= 1e-2
 
 
-def test_hgrn2_gate_spread_beyond_range_is_reported(lr):
-    """A chunk whose gates multiply below 2^-160 sets LR_ERR_RANGE."""
+def small_gates(p, kind, seed):
+    """Gates whose log2 products over a 64-step chunk fall far below what one
+    reference point per chunk can factor (the page's lower bound may be 0):
+    the kernel splits such chunks into virtual chunks of 32, 16, .. steps."""
+    g = torch.Generator().manual_seed(seed)
+    shape = p["g"].shape
+    if kind == "const_0.1":            # 64 log2(0.1) = -212 per chunk
+        gt = torch.full(shape, 0.1)
+    elif kind == "uniform_0_0.2":      # heavy tail towards 0
+        gt = 0.2 * torch.rand(shape, generator=g)
+    elif kind == "lb0_wide":           # lb = 0, f ~ N(0, 3): sigmoid(f) down to ~1e-5
+        gt = torch.sigmoid(3.0 * torch.randn(shape, generator=g))
+    elif kind == "mixed":              # per-channel mix of slow, fast and vanishing gates
+        gt = torch.sigmoid(torch.randn(shape, generator=g) * 2.0 + 2.0)
+        gt[..., 1::3] = 0.02
+        gt[..., 2::7] = 0.0            # a reset every step
+    else:
+        raise ValueError(kind)
+    p["g"] = gt.to(torch.bfloat16)
+    return p
+
+
+@pytest.mark.parametrize("kind", ["const_0.1", "uniform_0_0.2", "lb0_wide", "mixed"])
+def test_hgrn2_small_gates_match_the_oracle(lr, kind):
+    p = small_gates(wl.hgrn2_inputs(1, 448, 2, 128, seed=10, with_S0=True), kind, seed=11)
+    check(lr, p, S0=0.1 * p["S0"])
+
+
+def test_hgrn2_steep_chunk_in_one_block_only(lr):
+    """One thread block (batch row 1, head 1, value channels 64..127) meets
+    steep gates late in the sequence; the call's second launch redoes that
+    block alone and every other block keeps its first-pass results.  The same
+    workspace then serves a call with ordinary gates."""
+    B, L, H = 2, 640, 3
+    p = wl.hgrn2_inputs(B, L, H, 128, seed=14, with_S0=True)
+    g = p["g"].float()
+    g[1, 400:, 128 + 64:256] = 0.01
+    p["g"] = g.to(torch.bfloat16)
+    ws = torch.empty(lr.lr_hgrn2_workspace_size(B, L, H, 128, 128, lr.LR_BF16), dtype=torch.uint8,
+                     device="cuda")
+    assert ws.numel() == 256 + B * H * 2 * 8
+    S0 = 0.1 * p["S0"]
+    c = {n: p[n].cuda() for n in ("q", "k", "v", "g")}
+    o, Sf = lr.hgrn2(c["q"], c["k"], c["v"], c["g"], H=H, S0=S0.cuda(), workspace=ws)
+    assert lr.status(ws) == 0
+    orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], p["g"], H, S0=S0)
+    assert rel_err(o.float().cpu(), orf) <= TOL and rel_err(Sf.cpu(), Srf) <= TOL
+    q = wl.hgrn2_inputs(B, L, H, 128, seed=15)
+    o2, S2 = lr.hgrn2(*(q[n].cuda() for n in ("q", "k", "v", "g")), H=H, workspace=ws)
+    assert lr.status(ws) == 0
+    orf, Srf = oracle.hgrn2(q["q"], q["k"], q["v"], q["g"], H)
+    assert rel_err(o2.float().cpu(), orf) <= TOL and rel_err(S2.cpu(), Srf) <= TOL
+
+
+def test_hgrn2_small_gates_preact_lower_bound_zero(lr):
+    """The page's default configuration: lb = 0 on pre-activation gates."""
+    p = wl.hgrn2_inputs(1, 320, 2, 128, seed=12)
+    f = (3.0 * torch.randn(p["g"].shape, generator=torch.Generator().manual_seed(13))).to(torch.bfloat16)
+    q, k, v = (p[n].cuda() for n in ("q", "k", "v"))
+    o, Sf = lr.hgrn2(q, k, v, f.cuda(), H=2, gate_lb=0.0)
+    torch.cuda.synchronize()
+    assert lr.status() == 0
+    gref = torch.sigmoid(f.double())
+    orf, Srf = oracle.hgrn2(p["q"], p["k"], p["v"], gref, 2)
+    assert rel_err(o.float().cpu(), orf) <= TOL and rel_err(Sf.cpu(), Srf) <= TOL
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")])
+def test_hgrn2_gate_not_finite_is_reported(lr, bad):
+    """A gate that is not a finite number sets LR_ERR_RANGE."""
     p = wl.hgrn2_inputs(1, 64, 1, 128, seed=10)
-    p["g"] = torch.full_like(p["g"], 0.1)   # 64 steps of log2(0.1) = -212
-    q, k, v, g = (p[n].cuda() for n in ("q", "k", "v", "g"))
-    lr.hgrn2(q, k, v, g, H=1)
+    g = p["g"].clone()
+    g[0, 17, 5] = bad
+    q, k, v = (p[n].cuda() for n in ("q", "k", "v"))
+    lr.hgrn2(q, k, v, g.cuda(), H=1)
     assert lr.status() == lr.LR_ERR_RANGE
     assert lr.status() == 0
 
