@@ -88,35 +88,48 @@ def step_configs(only=None, seq_len=None):
 # costs one exp2 on the MUFU pipe (the discretised decay) and four fp32 ops on
 # the FMA pipe (the decay argument, the input product, the state FMA, the
 # readout FMA).  At 128 fp32 lanes and 32 exp2 results per clock per SM the
-# two pipes cap the update at min(128/4, 32/1) = 32 elements per clock per SM;
-# with 152 SMs at the 2070 MHz maximum clock that is 10.07 T elements/s.
+# two pipes cap the update at min(128/4, 32/1) = 32 elements per clock per SM.
 # The powers form of the decays (A_log on the multi-scale lattice) moves most
 # exp2s off the MUFU pipe but keeps four fp32 ops per element (a power-chain
 # multiply replaces the decay argument), so the same 32 per clock bound it.
-ALU_SMS = 152
-ALU_MAX_MHZ = 2070
+# The SM count is the device's; the clock is the maximum SM clock that
+# nvidia-smi reports during the timed region (2070 MHz on a GB300 when no
+# record could be taken).
 ALU_ELEMS_PER_CLK_SM = 32
+FALLBACK_MAX_MHZ = 2070
 
 
-def alu_peak_gelem() -> float:
-    return ALU_SMS * ALU_MAX_MHZ * 1e6 * ALU_ELEMS_PER_CLK_SM / 1e9
+def alu_peak(sms: int, max_mhz) -> tuple:
+    mhz = float(max_mhz) if max_mhz else float(FALLBACK_MAX_MHZ)
+    src = (f"derived: {sms} SMs (device attribute) x {mhz:.0f} MHz "
+           f"({'nvidia-smi clocks.max.sm' if max_mhz else 'GB300 maximum, no clock record'}) "
+           f"x {ALU_ELEMS_PER_CLK_SM} state updates/clk/SM")
+    return sms * mhz * 1e6 * ALU_ELEMS_PER_CLK_SM / 1e9, src
 
 
-def kernel_roofline(cfg: wl.Config, a: dict, ms: float, peaks: dict) -> dict:
-    """Roofline entry of one scan's kernel for one launch of ``ms``."""
+def kernel_roofline(cfg: wl.Config, a: dict, ms: float, peaks: dict, alu=None) -> dict:
+    """Roofline entry of one scan's kernel for one launch of ``ms``: HBM
+    bandwidth of its algorithmic bytes against the measured copy peak, and
+    for the selective scan also its state updates against the ALU peak
+    ``alu`` = (Gelem/s, how it was derived), the bound it really meets."""
     sec = ms * 1e-3
-    if cfg.form == "selective":
+    gbs = a["bytes"] / sec / 1e9
+    e = {"kernel": cfg.name, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": traffic_for(cfg),
+         "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"}
+    if cfg.form == "selective" and alu is not None:
         ach = a["units"] * cfg.N / sec / 1e9
-        peak = alu_peak_gelem()
-        return {"kernel": cfg.name, "bound": "alu", "achieved": ach, "peak": peak,
-                "unit": "Gelem/s", "frac": ach / peak, "traffic": traffic_for(cfg),
-                "peak_source": "derived: 152 SMs x 2070 MHz x 32 state updates/clk/SM",
-                "decay_form": "powers: the workload's A_log is on the multi-scale lattice, "
-                              "checked per warp in the kernel"}
-    ach = a["bytes"] / sec / 1e9
-    return {"kernel": cfg.name, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": traffic_for(cfg),
-            "peak_source": peaks["source"]}
+        e["alu"] = {"bound": "alu", "achieved": ach, "peak": alu[0], "unit": "Gelem/s",
+                    "frac": ach / alu[0], "peak_source": alu[1]}
+        e["limited_by"] = "alu (issue-bound state updates; HBM is not the binding limit)"
+        e["decay_form"] = ("powers: the workload's A_log is on the multi-scale lattice, "
+                           "checked per warp in the kernel")
+    if cfg.form == "hgrn2" and a["flops"]:
+        tf = a["flops"] / sec / 1e12
+        e["tensor"] = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops_sustained"],
+                       "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops_sustained"],
+                       "peak_source": peaks["source"] + " (bf16_tflops_sustained)"}
+    return e
 
 
 # ----------------------------------------------------------------------------
@@ -250,6 +263,7 @@ def cpu_baseline(cfgs, repeats=1, samples=None, single_thread=False) -> dict:
     if samples is None:
         samples = [(cfg, *oracle_sample(cfg)) for cfg in cfgs]
     rates = {}
+    sample_s = 0.0
     for cfg, kind, args, units in samples:
         run_oracle(kind, args)  # warm (page-in, thread pool)
         t0 = time.perf_counter()
@@ -257,13 +271,14 @@ def cpu_baseline(cfgs, repeats=1, samples=None, single_thread=False) -> dict:
             run_oracle(kind, args)
         dt = (time.perf_counter() - t0) / repeats
         rates[cfg.name] = units / dt
+        sample_s += dt
     total_units = sum(algorithmic(c)["units"] for c in cfgs)
     step_time = sum(algorithmic(c)["units"] / rates[c.name] for c in cfgs)
     desc = "; ".join(f"{c.name}: {u} of {algorithmic(c)['units']} units"
                      for c, _, _, u in samples)
     out = {"value": total_units / step_time, "unit": UNIT, "cores": cores, "kind": "oracle",
            "sample": "whole sequences of a channel/head subset of batch row 0 -- " + desc,
-           "per_scan_units_per_s": rates}
+           "per_scan_units_per_s": rates, "sample_ms": sample_s * 1e3}
     if single_thread:
         # the same samples on one host thread (one timed run each)
         rates1 = {}
@@ -375,31 +390,62 @@ def off_lattice_A_log(A_log: torch.Tensor) -> torch.Tensor:
     return A_log + 0.05 * torch.randn(A_log.shape, device=A_log.device, generator=g)
 
 
-def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
-    """Scans outside the step, timed the same way (inputs larger than L2,
-    CUDA events on the launching stream): the selective workload with
-    general (off-lattice) decays, the MinMax recurrence at the RG-LRU
-    workload's shape, the pre-activation gate forms and fp32 HGRN2."""
-    def timed(fn):
+def extra_timings(lr, dev, peaks, alu, reps: int = 20) -> list:
+    """Scans outside the step, timed the same way (CUDA events on the
+    launching stream, median of ``reps`` launches): the two oracle-sized
+    workloads (fp32 RG-LRU B2 L128 D64 and fp32 selective B2 L1024 D1536,
+    whose inputs fit in L2: timed with the 129 MB L2 flushed before every
+    launch, and the selective one also hot, launched back to back), the
+    selective workload with general (off-lattice) decays, the MinMax
+    recurrence at the RG-LRU workload's shape, the pre-activation gate forms
+    and fp32 HGRN2 (inputs larger than L2)."""
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn, flush=False):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(reps)]
         for a, b in ev:
+            if flush:
+                flush_buf.zero_()   # evicts the previous launch's lines from L2
             a.record()
             fn()
             b.record()
         torch.cuda.synchronize()
         return statistics.median(a.elapsed_time(b) for a, b in ev)
 
-    def entry(name, ms, units, by):
+    def entry(name, ms, units, by, l2=None):
         gbs = by / (ms * 1e-3) / 1e9
-        return {"workload": name, "ms": ms, "tok_ch_per_s": units / (ms * 1e-3), "gb_per_s": gbs,
-                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}}
+        d = {"workload": name, "ms": ms, "tok_ch_per_s": units / (ms * 1e-3), "gb_per_s": gbs,
+             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"]}}
+        if l2:
+            d["l2"] = l2
+        return d
 
     res = []
+    # the two small workloads (their inputs fit in L2)
+    for key in ("rglru_f32_small", "selective_f32"):
+        cfg = wl.WORKLOADS[key]
+        p = wl.make_inputs(cfg, device=dev)
+        ws = workspace_for(lr, cfg, dev)
+        fn = make_call(lr, cfg, p, ws=ws)
+        a = algorithmic(cfg)
+        modes = (("flushed", True), ("hot", False)) if cfg.form == "selective" else (("flushed", True),)
+        for mode, fl in modes:
+            ms = timed(fn, flush=fl)
+            e = entry(f"{cfg.name} ({mode} L2)", ms, a["units"], a["bytes"],
+                      l2="129 MB L2 flushed before every launch" if fl else
+                      "hot: inputs resident in L2 (launched back to back, no flush)")
+            if cfg.form == "selective":
+                e["roofline"] = kernel_roofline(cfg, a, ms, peaks, alu)
+                e["roofline"]["traffic"] = None
+            res.append(e)
+        check_calls(lr, [ws], torch.cuda.current_stream(dev), f"in the {cfg.name} timing")
+        del p, ws, fn
+    del flush_buf
     # the selective workload with A_log moved off the initialisation lattice
     # (as training moves it): the general one-exp-per-state decays
     cfg = wl.WORKLOADS["selective_bf16"]
@@ -407,7 +453,7 @@ def extra_timings(lr, dev, peaks, reps: int = 20) -> list:
     A_off = off_lattice_A_log(p["A_log"])
     ms = timed(lambda: lr.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], A_off, z=p["z"],
                                          Dskip=p["Dskip"], h0=p["h0"]))
-    rl = kernel_roofline(cfg, algorithmic(cfg), ms, peaks)
+    rl = kernel_roofline(cfg, algorithmic(cfg), ms, peaks, alu)
     rl["decay_form"] = "general: one exp2 per state (A_log off the lattice)"
     rl["traffic"] = None
     res.append({"workload": cfg.name + " A_log off the lattice", "ms": ms,
@@ -514,15 +560,20 @@ def gpu_arm(args):
     for fn in host_calls:
         fn()
     torch.cuda.synchronize()
-    e2e_steps = max(1, min(args.steps, 5))
+    # every step returns with its outputs in the caller's host buffers (each
+    # call synchronises); timed over up to 20 steps, per-step times kept
+    e2e_steps = max(3, min(args.steps, 20))
     barrier(world)
-    t0 = time.perf_counter()
     d2h = 0
+    e2e_ms = []
+    t0 = time.perf_counter()
     for _ in range(e2e_steps):
+        ts = time.perf_counter()
         d2h = 0
         for fn in host_calls:
             outs = fn()
             d2h += sum(t.numel() * t.element_size() for t in outs)
+        e2e_ms.append((time.perf_counter() - ts) * 1e3)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev) / e2e_steps
     del host_inputs, host_calls, host_outs
@@ -530,8 +581,10 @@ def gpu_arm(args):
     units_step = sum(a["units"] for a in alg)
     value = job_throughput(world, units_step, args.steps, total_ms)
     peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu = alu_peak(sms, clk.get("sm_max_mhz") if clk else None)
     dom = max(range(len(cfgs)), key=lambda j: per_scan[j]["ms"])
-    rooflines = [kernel_roofline(c, a, d["ms"], peaks) for c, a, d in zip(cfgs, alg, per_scan)]
+    rooflines = [kernel_roofline(c, a, d["ms"], peaks, alu) for c, a, d in zip(cfgs, alg, per_scan)]
     if args.a_log_off_lattice:
         for r in rooflines:
             if "decay_form" in r:
@@ -555,7 +608,12 @@ def gpu_arm(args):
         "roofline": roof,
         "rooflines": rooflines,
         "e2e": {"value": world * units_step / e2e_s, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "ms_per_step": e2e_s * 1e3,
+                "ms_per_step_median": statistics.median(e2e_ms),
+                "ms_per_step_min": min(e2e_ms), "ms_per_step_max": max(e2e_ms),
+                "path": "lr_*_fwd on pinned host buffers: the library copies each chunk in, "
+                        "scans it and copies the outputs back (wall clock, host timer)"},
         "gpu_launches": len(cfgs) * args.steps,
         "clocks": clk,
     }
@@ -563,7 +621,7 @@ def gpu_arm(args):
         line["config"]["selective_A_log"] = "moved off the initialisation lattice (profiling case)"
     if not args.seq_len and not args.only and not args.no_extras:
         line["decode"] = decode_timings(lr, cfgs, dev)
-        line["extra"] = extra_timings(lr, dev, peaks)
+        line["extra"] = extra_timings(lr, dev, peaks, alu)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfgs, single_thread=True)
     if rank == 0:
@@ -587,7 +645,7 @@ def load_peaks() -> dict:
 
 # CUDA sources each scan's kernel is compiled from.
 KERNEL_SOURCES = {"rglru": ("lr_diag_scan.cu", "lr_device.cuh"),
-                  "selective": ("lr_diag_scan.cu", "lr_device.cuh"),
+                  "selective": ("lr_selective.cuh", "lr_selective.cu", "lr_device.cuh"),
                   "hgrn2": ("lr_hgrn2.cu", "lr_device.cuh")}
 
 
@@ -629,22 +687,29 @@ def reference_arm(args):
     cfgs = step_configs(args.only, args.seq_len)
     samples = [(cfg, *oracle_sample(cfg)) for cfg in cfgs]
     cb = None
-    vals = []
+    vals, sample_ms = [], []
     for _ in range(args.warmup):
         cpu_baseline(cfgs, samples=samples)
     for _ in range(args.steps):
         cb = cpu_baseline(cfgs, samples=samples)
         vals.append(cb["value"])
+        sample_ms.append(cb["sample_ms"])
     value = statistics.mean(vals)
     cb["value"] = value
+    full_units = sum(algorithmic(c)["units"] for c in cfgs)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": sum(algorithmic(c)["units"] for c in cfgs) / value * 1e3,
+        # one step is the bounded sample of every scan: this is its measured
+        # wall time; the rate is that of the sample
+        "ms_per_step": statistics.mean(sample_ms),
+        "ms_per_step_kind": "measured: one step = the bounded sample of each scan (cpu_baseline.sample)",
+        "full_workload_ms_per_step_extrapolated": full_units / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generators with the pages' layer distributions)",
         "config": {"workload": " + ".join(c.name for c in cfgs),
-                   "l2": "n/a (host cores)", "parallelism": "host threads"},
+                   "l2": "n/a (host cores)", "parallelism": "host threads",
+                   "sample": "whole sequences of a channel/head subset of batch row 0 of each scan"},
         "cpu_baseline": cb,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -129,7 +129,7 @@ int lr_check_status(void *workspace, lr_stream_t stream);
  * Parallel pieces: the kernel cuts each sequence into pieces that run in
  * parallel.  A piece that starts inside the sequence rebuilds its starting
  * state from the preceding steps back to where the carried state has decayed
- * below 2^-12 (bf16 I/O) or 2^-32 (fp32 I/O) of its size, or takes it from
+ * below 2^-10 (bf16 I/O) or 2^-32 (fp32 I/O) of its size, or takes it from
  * the preceding pieces (see lr_set_selective_warmup); the history left out
  * is below that share, inside the tolerances above.  Results therefore
  * depend on the rounding of the piece boundaries, which depend on the
@@ -448,14 +448,19 @@ int lr_set_split_override(int splits);
  * Tuning / test knob of the selective scan.  The kernel cuts sequences into
  * pieces that run in parallel.  A piece that starts inside a sequence first
  * rebuilds the state reached just before it from the preceding steps, back
- * to where every channel's slowest decay has fallen below 2^-12 (bf16 I/O) or
+ * to where every channel's slowest decay has fallen below 2^-10 (bf16 I/O) or
  * 2^-32 (fp32 I/O), so that the history left out contributes less than that
  * share of the state's size (a "warm-up"), when that window lies within
  * `max_steps` steps; otherwise it runs from zero, takes its carry from the
  * preceding pieces by decoupled look-back and corrects its outputs by the
- * carry's contribution (to the same cut-off).  0 disables the warm-up (every
- * carry by look-back).  Default 2048.  Process-wide, not thread-safe.
- * Returns the previous setting.
+ * carry's contribution (to the same cut-off).  With warm-ups on, a warp
+ * that has run out of work splits off the back half of the largest range
+ * still unclaimed and warms up to its start (so results can differ between
+ * runs within the cut-off).  0 disables the warm-up (every carry by
+ * look-back, a fixed partition); a negative value restores the automatic
+ * setting: 2048 steps for bf16 I/O, 0 for fp32 I/O (whose 2^-32 window is
+ * about as long as the pages' sequences).  Process-wide, not thread-safe.
+ * Returns the previous setting (-1: automatic).
  */
 int64_t lr_set_selective_warmup(int64_t max_steps);
 

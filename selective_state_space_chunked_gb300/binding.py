@@ -130,8 +130,9 @@ def lr_set_host_chunk_steps(steps: int) -> int:
 
 
 def lr_set_selective_warmup(max_steps: int) -> int:
-    """Longest warm-up of the selective scan's pieces (0 = carries by
-    look-back only); returns the previous setting."""
+    """Longest warm-up of the selective scan's pieces in steps (0 = carries
+    by look-back only, negative = automatic: 2048 for bf16 I/O, 0 for fp32);
+    returns the previous setting (-1 = automatic)."""
     return int(_lib.lr_set_selective_warmup(int(max_steps)))
 
 

@@ -16,7 +16,7 @@ namespace lr {
 int g_split_override = 0;
 int g_withheld_split = -1;
 int g_withheld_timeout_ms = 1000;
-int64_t g_selective_warmup_steps = 2048;
+int64_t g_selective_warmup_steps = -1;   // automatic
 
 namespace {
 std::atomic<unsigned long long> g_stamp{0};
@@ -210,7 +210,8 @@ int64_t lr_set_host_chunk_steps(int64_t steps) {
 
 int64_t lr_set_selective_warmup(int64_t max_steps) {
     const int64_t prev = lr::g_selective_warmup_steps;
-    lr::g_selective_warmup_steps = max_steps > 0 ? (max_steps < (int64_t(1) << 30) ? max_steps : (int64_t(1) << 30)) : 0;
+    lr::g_selective_warmup_steps =
+        max_steps < 0 ? -1 : (max_steps < (int64_t(1) << 30) ? max_steps : (int64_t(1) << 30));
     return prev;
 }
 

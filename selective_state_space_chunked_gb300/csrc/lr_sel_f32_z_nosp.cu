@@ -1,0 +1,9 @@
+// lr_sel_f32_z_nosp.cu -- one compiled variant of the selective scan kernel:
+// fp32 I/O, with the silu(z) gate, dt taken as delta (see lr_selective.cuh).
+#include "lr_selective.cuh"
+
+namespace lr {
+namespace sel {
+LR_SEL_DEFINE(f32_z_nosp, float, true, true, false)
+}  // namespace sel
+}  // namespace lr

@@ -263,3 +263,16 @@ def test_minmax_step_validation_codes(lr, kw, code):
     a = dict(r=FAKE, s=FAKE, x_in=FAKE, x_out=FAKE, y=FAKE, B=2, D=64, io=1, stream=None)
     a.update(kw)
     assert lr.lr_minmax_scan_step(*a.values()) == code
+
+
+def test_selective_warmup_knob_round_trips(lr):
+    """The warm-up limit is process-wide: negative means automatic (reported
+    as -1), 0 turns warm-ups off, larger values are capped at 2^30 steps."""
+    prev = lr.lr_set_selective_warmup(5000)
+    try:
+        assert lr.lr_set_selective_warmup(0) == 5000
+        assert lr.lr_set_selective_warmup(-7) == 0
+        assert lr.lr_set_selective_warmup(1 << 40) == -1
+        assert lr.lr_set_selective_warmup(-1) == 1 << 30
+    finally:
+        lr.lr_set_selective_warmup(prev)

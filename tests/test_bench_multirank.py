@@ -72,3 +72,32 @@ def test_reference_arm_prints_on_rank0_only():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    # ms_per_step is the measured time of the sampled step; the whole
+    # workload's time is labelled as extrapolated
+    assert d["ms_per_step"] == pytest.approx(d["cpu_baseline"]["sample_ms"], rel=1.0)
+    assert d["ms_per_step_kind"].startswith("measured")
+    assert d["full_workload_ms_per_step_extrapolated"] >= d["ms_per_step"]
+
+
+def test_roofline_entries_lead_with_hbm():
+    """Every scan's roofline entry is its HBM fraction; the selective scan's
+    also carries the ALU fraction against a peak derived from the SM count
+    and clock it is given, HGRN2's the tensor fraction."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from selective_state_space_chunked_gb300 import workloads as wl
+    peaks = {"hbm_gbs": 8000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0,
+             "source": "test"}
+    alu = bench.alu_peak(100, 2000.0)
+    assert alu[0] == pytest.approx(100 * 2000e6 * 32 / 1e9)
+    assert "100 SMs" in alu[1]
+    assert bench.alu_peak(152, None)[0] == pytest.approx(152 * 2070e6 * 32 / 1e9)
+    sel = wl.WORKLOADS["selective_bf16"]
+    a = bench.algorithmic(sel)
+    e = bench.kernel_roofline(sel, a, 1.0, peaks, alu)
+    assert e["bound"] == "hbm" and e["frac"] == pytest.approx(a["bytes"] / 1e-3 / 1e9 / 8000.0)
+    assert e["alu"]["frac"] == pytest.approx(a["units"] * sel.N / 1e-3 / 1e9 / alu[0])
+    hg = wl.WORKLOADS["hgrn2_bf16"]
+    e = bench.kernel_roofline(hg, bench.algorithmic(hg), 0.1, peaks, alu)
+    assert e["bound"] == "hbm" and "alu" not in e
+    assert e["tensor"]["frac"] == pytest.approx(bench.algorithmic(hg)["flops"] / 1e-4 / 1e12 / 1600.0)

@@ -33,7 +33,7 @@ def lr():
     return binding
 
 
-WARMUP_DEFAULT = 2048
+WARMUP_DEFAULT = -1   # automatic: 2048 steps for bf16 outputs, look-back for fp32
 
 
 @pytest.fixture(autouse=True)

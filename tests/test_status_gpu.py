@@ -33,11 +33,11 @@ def lr():
 def _knobs(lr):
     lr.lr_set_split_override(0)
     lr.lr_test_withhold_split(-1, 1000)
-    lr.lr_set_selective_warmup(2048)
+    lr.lr_set_selective_warmup(-1)
     yield
     lr.lr_set_split_override(0)
     lr.lr_test_withhold_split(-1, 1000)
-    lr.lr_set_selective_warmup(2048)
+    lr.lr_set_selective_warmup(-1)
 
 
 def cuda(d):
