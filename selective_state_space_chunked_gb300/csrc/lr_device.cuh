@@ -80,6 +80,15 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 }
 
 // Makes mbarrier initialisation visible to the async proxy (TMA).
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start before the grid it follows has finished;
+// grid_dependency_wait() blocks until that grid has completed and its memory
+// is visible (it returns at once in a grid launched the ordinary way), and
+// launch_dependents() lets the following grid start launching once every
+// block of this grid has called it or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

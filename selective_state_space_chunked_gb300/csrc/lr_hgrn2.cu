@@ -401,9 +401,11 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (SPLIT) {
+        grid_dependency_wait();   // launched as the first pass's dependent
         if (redo[blockIdx.x] != sref.stamp) return;   // the first pass was right
-    } else if (tid == 0 && blockIdx.x == 0) {
-        status_begin(sref);
+    } else {
+        launch_dependents();   // the redo pass may launch; its blocks wait for this grid
+        if (tid == 0 && blockIdx.x == 0) status_begin(sref);
     }
     if ((smem_u32(sm) & 1023u) != 0) {  // swizzled tiles need a 1024-byte aligned base
         if (tid == 0) status_report(sref, LR_ERR_CUDA);
@@ -825,11 +827,24 @@ int hgrn2_launch(const void *q, const void *k, const void *v, const void *g, con
         static_cast<int>(H), n_chunks, lb, timeout, sref, redo);
     if (cudaGetLastError() != cudaSuccess) return LR_ERR_CUDA;
     if (preact && lb >= kLbNoSplit) return LR_OK;
+    // the redo pass as a programmatic dependent launch: its launch overlaps the
+    // first pass, and its blocks wait for the first pass's completion before
+    // they read the redo words
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(hg::THREADS);
+    cfg.dynamicSmemBytes = hg::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     auto second = preact ? hgrn2_chunk_kernel<true, true> : hgrn2_chunk_kernel<false, true>;
-    second<<<static_cast<unsigned>(grid), hg::THREADS, hg::SMEM, stream>>>(
-        mq, mk, mv, mg, S0, S_final, static_cast<__nv_bfloat16 *>(o), static_cast<int>(L),
-        static_cast<int>(H), n_chunks, lb, timeout, sref, redo);
-    return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, second, mq, mk, mv, mg, S0, S_final,
+                                             static_cast<__nv_bfloat16 *>(o), static_cast<int>(L),
+                                             static_cast<int>(H), n_chunks, lb, timeout, sref, redo);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 
 }  // namespace lr

@@ -1324,6 +1324,10 @@ __global__ void __launch_bounds__(kWpb * 32, SelCfg<IO, CPL>::MINB)
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_ticket;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (STEAL)
+        launch_dependents();   // the launch for deferred shares may start; it waits for this grid
+    else if (a.deferred)
+        grid_dependency_wait();   // the stealing launch has completed and its writes are visible
     Ring rg{smem + warp * Cf::WARP_SMEM, nullptr, 0, true};
     rg.full = reinterpret_cast<uint64_t *>(rg.base + Cf::OFF_BAR);
     if (threadIdx.x == 0) {
@@ -1386,9 +1390,21 @@ int launch_variant(const CUtensorMap *mp, const SelArgs &a, int grid, cudaStream
     if (cudaGetLastError() != cudaSuccess) return LR_ERR_CUDA;
     SelArgs b = a;
     b.deferred = 1;
-    selective_scan_kernel<IO, ACC, HZ, SP, false>
-        <<<static_cast<unsigned>(grid), kWpb * 32, smem, stream>>>(mp[0], mp[1], mp[2], mp[3], mp[4], mp[5], b);
-    return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
+    // a programmatic dependent launch: it starts launching while the stealing
+    // grid runs, and its blocks wait for that grid before reading the marks
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kWpb * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, selective_scan_kernel<IO, ACC, HZ, SP, false>, mp[0], mp[1], mp[2],
+                                             mp[3], mp[4], mp[5], b);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 
 // Resident blocks per SM of variant (IO, HZ, SP) (both forms; sets their
