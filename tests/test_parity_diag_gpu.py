@@ -186,11 +186,12 @@ def test_selective_optional_inputs(lr, variant):
     check_sel(lr, p, "f32", **over)
 
 
-@pytest.mark.parametrize("warmup", [WARMUP_DEFAULT, 0])
+@pytest.mark.parametrize("warmup", [WARMUP_DEFAULT, 2048, 0])
 @pytest.mark.parametrize("splits", [2, 3, 5])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_selective_forced_time_splits(lr, splits, io, warmup):
-    """Pieces that start inside a sequence.  With the warm-up (default) each
+    """Pieces that start inside a sequence.  With the warm-up (the default for
+    bf16, forced by 2048 for fp32 too) each
     rebuilds its state over the preceding steps -- here all the way from the
     sequence start, since the slowest channels' horizon is longer than the
     sequence; with it disabled the carry comes by decoupled look-back and the
@@ -201,7 +202,7 @@ def test_selective_forced_time_splits(lr, splits, io, warmup):
     check_sel(lr, p, io)
 
 
-@pytest.mark.parametrize("warmup", [WARMUP_DEFAULT, 0])
+@pytest.mark.parametrize("warmup", [2048, 0])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_selective_warmup_stops_at_its_horizon(lr, io, warmup):
     """Pieces of 1500 steps over the four decay scales of a 64-channel
@@ -212,6 +213,25 @@ def test_selective_warmup_stops_at_its_horizon(lr, io, warmup):
     p = wl.selective_inputs(1, 6000, 64, seed=31, io=io, with_h0=True)
     lr.lr_set_split_override(4)
     lr.lr_set_selective_warmup(warmup)
+    check_sel(lr, p, io)
+
+
+@pytest.mark.parametrize("splits", [2, 3])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_selective_work_stealing(lr, io, splits):
+    """One 64-channel chain of 2048 tiles shared by 2 or 3 warps: the warp
+    that starts at the sequence start needs no warm-up and finishes first, so
+    it splits off the back half of another warp's unclaimed range (ranges of
+    at least 64 tiles are split), warms up to its start and runs it.  Warm-ups
+    are on for both dtypes, so the fp32 case runs at its 2^-32 cut-off.  The
+    whole output and the final state match the oracle."""
+    p = wl.selective_inputs(1, 16384, 64, seed=40 + splits, io=io, with_h0=True)
+    # steps about 7x smaller than the workload's: the warm-up horizons (about
+    # 280 tiles for bf16, 900 for fp32) make the shares that warm up finish
+    # late enough that the first warp finds a remainder worth splitting
+    p["dt"] = (p["dt"].float() - 2.0).to(p["dt"].dtype)
+    lr.lr_set_split_override(splits)
+    lr.lr_set_selective_warmup(1 << 20)   # no share falls back to look-back
     check_sel(lr, p, io)
 
 
