@@ -490,6 +490,19 @@ def extra_timings(lr, dev, peaks, alu, reps: int = 20) -> list:
     return res
 
 
+def launches_per_call(cfg: wl.Config) -> int:
+    """Kernels one call of a workload's scan launches (the library's rules):
+    the RG-LRU scan one; the selective scan two with warm-ups (the default for
+    bf16 outputs: the stealing launch and the launch for deferred shares), one
+    without; HGRN2's tensor-core path two (first pass and redo pass), its
+    general path one.  The ncu launch list in profiles/ confirms the count."""
+    if cfg.form == "rglru":
+        return 1
+    if cfg.form == "selective":
+        return 2 if cfg.io == "bf16" else 1
+    return 2 if (cfg.io == "bf16" and cfg.head_dim == 128) else 1
+
+
 def input_bytes(p) -> int:
     return sum(t.numel() * t.element_size() for t in p.values() if torch.is_tensor(t))
 
@@ -614,7 +627,7 @@ def gpu_arm(args):
                 "ms_per_step_min": min(e2e_ms), "ms_per_step_max": max(e2e_ms),
                 "path": "lr_*_fwd on pinned host buffers: the library copies each chunk in, "
                         "scans it and copies the outputs back (wall clock, host timer)"},
-        "gpu_launches": len(cfgs) * args.steps,
+        "gpu_launches": sum(launches_per_call(c) for c in cfgs) * args.steps,
         "clocks": clk,
     }
     if args.a_log_off_lattice:
