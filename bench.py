@@ -481,10 +481,10 @@ def extra_timings(lr, dev, peaks, alu, reps: int = 20) -> list:
     res.append(entry(cfg.name + " gate_lb=0.2", timed(lambda: lr.hgrn2(
         p["q"], p["k"], p["v"], p["g"], H=p["H"], gate_lb=0.2)),
         algorithmic(cfg)["units"], algorithmic(cfg)["bytes"]))
-    # fp32 I/O at the same shape: the step-by-step CUDA-core kernel
+    # fp32 I/O at the same shape: the split-bf16 tensor-core kernel
     pf = {n: p[n].float() for n in ("q", "k", "v", "g")}
     del p
-    res.append(entry(f"hgrn2_f32_B{cfg.B}_L{cfg.L}_H{cfg.H}_d{cfg.head_dim} general kernel",
+    res.append(entry(f"hgrn2_f32_B{cfg.B}_L{cfg.L}_H{cfg.H}_d{cfg.head_dim} split-bf16 tensor-core kernel",
                      timed(lambda: lr.hgrn2(pf["q"], pf["k"], pf["v"], pf["g"], H=cfg.H)),
                      algorithmic(cfg)["units"], 2 * algorithmic(cfg)["bytes"]))
     return res

@@ -142,6 +142,10 @@ int validate_hgrn2(const void *q, const void *k, const void *v, const void *g, c
 bool hgrn2_tensor_path(int64_t dk, int64_t dv, int64_t chunk, lr_dtype io) {
     return dk == 128 && dv == 128 && chunk == 64 && io == LR_BF16;
 }
+// fp32 I/O on the tensor cores (split bf16 operands): 128 x 128 heads, chunk 64
+bool hgrn2_f32_tensor_path(int64_t dk, int64_t dv, int64_t chunk, lr_dtype io) {
+    return dk == 128 && dv == 128 && chunk == 64 && io == LR_F32;
+}
 
 int validate_minmax(const void *r, const void *s, const float *x0, const void *y, const float *x_final,
                     int64_t B, int64_t L, int64_t D, lr_dtype io) {
@@ -327,6 +331,8 @@ int lr_hgrn2_fwd(const void *q, const void *k, const void *v, const void *g, con
     if ((rc = lr::hgrn2_workspace(B, L, H, &need)) != LR_OK) return rc;
     if (workspace == nullptr || ws_bytes < need) return LR_ERR_WORKSPACE;
     if (misaligned(workspace)) return LR_ERR_MISALIGNED;
+    if (hgrn2_f32_tensor_path(dk, dv, chunk, io))
+        return lr::hgrn2_f32_launch(q, k, v, g, S0, o, S_final, B, L, H, workspace, st, false, 0.0f);
     if (!hgrn2_tensor_path(dk, dv, chunk, io))
         return lr::hgrn2_general_launch(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, io == LR_BF16,
                                         false, 0.0f, workspace, st);
@@ -446,6 +452,8 @@ extern "C" int lr_hgrn2_preact_fwd(const void *q, const void *k, const void *v, 
     if ((rc = lr::hgrn2_workspace(B, L, H, &need)) != LR_OK) return rc;
     if (workspace == nullptr || ws_bytes < need) return LR_ERR_WORKSPACE;
     if (misaligned(workspace)) return LR_ERR_MISALIGNED;
+    if (hgrn2_f32_tensor_path(dk, dv, chunk, io))
+        return lr::hgrn2_f32_launch(q, k, v, f, S0, o, S_final, B, L, H, workspace, st, true, lb);
     if (!hgrn2_tensor_path(dk, dv, chunk, io))
         return lr::hgrn2_general_launch(q, k, v, f, S0, o, S_final, B, L, H, dk, dv, io == LR_BF16,
                                         true, lb, workspace, st);

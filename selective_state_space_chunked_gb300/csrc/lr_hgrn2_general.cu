@@ -87,7 +87,8 @@ __global__ void __launch_bounds__(kNT, 1)
                          const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                          const IO *__restrict__ g, const float *__restrict__ S0,
                          IO *__restrict__ o, float *__restrict__ S_final, int L, int H, int dk,
-                         int dv, int nrb, float lb, uint64_t timeout_ns, StatusRef sref) {
+                         int dv, int nrb, float lb, uint64_t timeout_ns, StatusRef sref,
+                         const unsigned long long *__restrict__ redo) {
     using C = GenCfg<P, CPT, RT>;
     constexpr int kCPT = CPT, kRT = RT;
     constexpr int KB = C::KB, RB = C::RB, TC = C::TC, VT = C::VT;
@@ -101,9 +102,11 @@ __global__ void __launch_bounds__(kNT, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(os + VT);    // [NB]: chunk staged
 
     const int tid = threadIdx.x;
+    const int bh = blockIdx.x / nrb, rb = blockIdx.x - bh * nrb;
+    // re-running the heads a tensor-core pass marked (with that call's stamp)
+    if (redo != nullptr && redo[bh] != sref.stamp) return;
     if (tid == 0 && blockIdx.x == 0) status_begin(sref);
     const int p = tid % P, rg = tid / P;
-    const int bh = blockIdx.x / nrb, rb = blockIdx.x - bh * nrb;
     const int b = bh / H, h = bh - b * H;
     const int row0 = rb * RB;
     const int rbv = min(RB, dv - row0);      // rows of this block inside dv
@@ -275,7 +278,7 @@ inline bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr
 template <typename IO, int P, int CPT, int RT>
 int launch_p(const void *q, const void *k, const void *v, const void *g, const float *S0, void *o,
              float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv, bool pre,
-             float lb, StatusRef st, cudaStream_t stream) {
+             float lb, StatusRef st, cudaStream_t stream, const unsigned long long *redo) {
     using C = GenCfg<P, CPT, RT>;
     const int nrb = static_cast<int>((dv + C::RB - 1) / C::RB);
     const int64_t grid = B * H * nrb;
@@ -305,7 +308,7 @@ int launch_p(const void *q, const void *k, const void *v, const void *g, const f
         mq, mk, mv, mg, static_cast<const IO *>(q), static_cast<const IO *>(k),
         static_cast<const IO *>(v), static_cast<const IO *>(g), S0, static_cast<IO *>(o), S_final,
         static_cast<int>(L), static_cast<int>(H), static_cast<int>(dk), static_cast<int>(dv), nrb, lb,
-        kDefaultTimeoutNs, st);
+        kDefaultTimeoutNs, st, redo);
     return cudaGetLastError() == cudaSuccess ? LR_OK : LR_ERR_CUDA;
 }
 
@@ -314,18 +317,18 @@ int launch_p(const void *q, const void *k, const void *v, const void *g, const f
 template <typename IO, int DKP>
 int launch_dk(const void *q, const void *k, const void *v, const void *g, const float *S0, void *o,
               float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv, bool pre,
-              float lb, StatusRef st, cudaStream_t stream) {
+              float lb, StatusRef st, cudaStream_t stream, const unsigned long long *redo) {
     int sms = 0;
     if (device_sm_count(&sms) != LR_OK) return LR_ERR_CUDA;
     auto blocks = [&](int rb) { return B * H * ((dv + rb - 1) / rb); };
     const int64_t want = 3 * int64_t(sms) / 2;
     if (DKP > 256 || blocks(2 * kNT / (DKP / 32)) >= want)
-        return launch_p<IO, DKP / 32, 32, 2>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
+        return launch_p<IO, DKP / 32, 32, 2>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream, redo);
     if constexpr (DKP <= 256) {
         if (blocks(kNT / (DKP / 32)) >= want)
             return launch_p<IO, DKP / 32, 32, 1>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb,
-                                                 st, stream);
-        return launch_p<IO, DKP / 16, 16, 1>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
+                                                 st, stream, redo);
+        return launch_p<IO, DKP / 16, 16, 1>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream, redo);
     }
     return LR_ERR_UNSUPPORTED;
 }
@@ -333,12 +336,12 @@ int launch_dk(const void *q, const void *k, const void *v, const void *g, const 
 template <typename IO>
 int launch_io(const void *q, const void *k, const void *v, const void *g, const float *S0, void *o,
               float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
-              bool pre, float lb, StatusRef st, cudaStream_t stream) {
-    if (dk <= 32) return launch_dk<IO, 32>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
-    if (dk <= 64) return launch_dk<IO, 64>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
-    if (dk <= 128) return launch_dk<IO, 128>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
-    if (dk <= 256) return launch_dk<IO, 256>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
-    return launch_dk<IO, 512>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream);
+              bool pre, float lb, StatusRef st, cudaStream_t stream, const unsigned long long *redo) {
+    if (dk <= 32) return launch_dk<IO, 32>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream, redo);
+    if (dk <= 64) return launch_dk<IO, 64>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream, redo);
+    if (dk <= 128) return launch_dk<IO, 128>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream, redo);
+    if (dk <= 256) return launch_dk<IO, 256>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream, redo);
+    return launch_dk<IO, 512>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, pre, lb, st, stream, redo);
 }
 
 }  // namespace
@@ -346,12 +349,13 @@ int launch_io(const void *q, const void *k, const void *v, const void *g, const 
 int hgrn2_general_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                          void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
                          int64_t dv, int io_bf16, bool preact, float lb, void *workspace,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const unsigned long long *redo, unsigned long long stamp) {
     if (B * H * dv == 0) return LR_OK;
-    const StatusRef st = call_status(workspace);
+    StatusRef st = call_status(workspace);
+    if (redo != nullptr) st.stamp = stamp;   // part of the call that marked the heads
     return io_bf16 ? launch_io<__nv_bfloat16>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, preact, lb,
-                                              st, stream)
-                   : launch_io<float>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, preact, lb, st, stream);
+                                              st, stream, redo)
+                   : launch_io<float>(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, preact, lb, st, stream, redo);
 }
 
 }  // namespace lr

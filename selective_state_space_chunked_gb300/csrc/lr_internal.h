@@ -102,10 +102,19 @@ bool encode_map_3d(CUtensorMap *tm, const void *base, CUtensorMapDataType type, 
                    uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2);
 
 // HGRN2 for fp32 I/O and head dims other than 128 x 128 (CUDA cores, step by step)
+// redo != NULL: only the heads whose redo word holds `stamp` run (the heads
+// a tensor-core pass of the same call marked), under that call's stamp.
 int hgrn2_general_launch(const void *q, const void *k, const void *v, const void *g, const float *S0,
                          void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
                          int64_t dv, int io_bf16, bool preact, float lb, void *workspace,
-                         cudaStream_t stream);
+                         cudaStream_t stream, const unsigned long long *redo = nullptr,
+                         unsigned long long stamp = 0);
+
+// HGRN2 with fp32 I/O, 128 x 128 heads, on the tensor cores (split bf16
+// operands); heads with steep chunks are re-run by the general kernel.
+int hgrn2_f32_launch(const void *q, const void *k, const void *v, const void *g, const float *S0, void *o,
+                     float *S_final, int64_t B, int64_t L, int64_t H, void *workspace, cudaStream_t stream,
+                     bool preact, float lb);
 
 // Single-token decode steps (plain one-pass kernels)
 int selective_step_launch(const void *x, const void *dt, const void *z, const void *Bm, const void *Cm,
