@@ -233,15 +233,6 @@ __global__ void __launch_bounds__(hf::NT, 1)
                 tma_load_3d(sm + QS, &tm_q, full, qcol, (c + 1) * C, b);
                 tma_load_3d(sm + KS, &tm_k, full, qcol, (c + 1) * C, b);
             }
-            // P = Q K^T
-#pragma unroll
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
-                umma3(tmem + T_P, umma_smem_desc(s_base + QH + off, 16, 1024),
-                      umma_smem_desc(s_base + QL + off, 16, 1024), umma_smem_desc(s_base + KH + off, 16, 1024),
-                      umma_smem_desc(s_base + KL + off, 16, 1024), IDESC_P, kk == 0);
-            }
-            umma_commit(mma);
         }
 
         // gates: cumulative log2 over this thread's 16 steps
@@ -258,6 +249,17 @@ __global__ void __launch_bounds__(hf::NT, 1)
         if (-acc > kQuarterSafe) flags[1] = 1;   // steep: the head is re-run step by step
         tot[fq * RB + fi] = acc;
         __syncthreads();
+        if (tid == 0) {   // P = Q K^T, after this thread's share of the gate work
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * 8192 + (kk & 3) * 32;
+                umma3(tmem + T_P, umma_smem_desc(s_base + QH + off, 16, 1024),
+                      umma_smem_desc(s_base + QL + off, 16, 1024), umma_smem_desc(s_base + KH + off, 16, 1024),
+                      umma_smem_desc(s_base + KL + off, 16, 1024), IDESC_P, kk == 0);
+            }
+            umma_commit(mma);
+        }
         float off = 0.0f, lc = 0.0f;
 #pragma unroll
         for (int q = 0; q < FQ; ++q) {
