@@ -71,16 +71,18 @@ def algorithmic(cfg: wl.Config) -> dict:
 STEP_WORKLOADS = ("rglru_bf16", "selective_bf16", "hgrn2_bf16")
 
 
-def step_configs(only=None, seq_len=None):
-    """The step's workloads; ``only`` keeps one form and ``seq_len`` shortens
-    the sequences (profiling cases: a launch of the same kernel on a smaller
-    input, never a benchmark number)."""
+def step_configs(only=None, seq_len=None, io=None):
+    """The step's workloads; ``only`` keeps one form, ``seq_len`` shortens
+    the sequences and ``io`` changes the I/O dtype (profiling cases: a launch
+    of a kernel on another input, never a benchmark number)."""
     import dataclasses
     cfgs = [wl.WORKLOADS[k] for k in STEP_WORKLOADS]
     if only:
         cfgs = [c for c in cfgs if c.form == only]
     if seq_len:
         cfgs = [dataclasses.replace(c, L=seq_len) for c in cfgs]
+    if io:
+        cfgs = [dataclasses.replace(c, io=io) for c in cfgs]
     return cfgs
 
 
@@ -513,7 +515,7 @@ def gpu_arm(args):
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
     from selective_state_space_chunked_gb300 import binding as lr
-    cfgs = step_configs(args.only, args.seq_len)
+    cfgs = step_configs(args.only, args.seq_len, args.io)
     inputs = [wl.make_inputs(c, device=dev) for c in cfgs]
     if args.a_log_off_lattice:
         for c, p in zip(cfgs, inputs):
@@ -632,7 +634,9 @@ def gpu_arm(args):
     }
     if args.a_log_off_lattice:
         line["config"]["selective_A_log"] = "moved off the initialisation lattice (profiling case)"
-    if not args.seq_len and not args.only and not args.no_extras:
+    if args.io:
+        line["config"]["io_override"] = f"{args.io} I/O (profiling case)"
+    if not args.seq_len and not args.only and not args.io and not args.no_extras:
         line["decode"] = decode_timings(lr, cfgs, dev)
         line["extra"] = extra_timings(lr, dev, peaks, alu)
     if rank == 0 and not args.no_cpu_baseline:
@@ -743,6 +747,8 @@ def main():
                     help="run one scan of the step (profiling case)")
     ap.add_argument("--seq-len", type=int, default=None,
                     help="shorter sequences for a profiling case (not a benchmark number)")
+    ap.add_argument("--io", choices=["bf16", "f32"], default=None,
+                    help="I/O dtype of the step's scans (a profiling case, not the workload)")
     ap.add_argument("--a-log-off-lattice", action="store_true",
                     help="selective A_log moved off the initialisation lattice (the general "
                          "decay form; a profiling case, not the workload)")
