@@ -496,13 +496,15 @@ def launches_per_call(cfg: wl.Config) -> int:
     """Kernels one call of a workload's scan launches (the library's rules):
     the RG-LRU scan one; the selective scan two with warm-ups (the default for
     bf16 outputs: the stealing launch and the launch for deferred shares), one
-    without; HGRN2's tensor-core path two (first pass and redo pass), its
-    general path one.  The ncu launch list in profiles/ confirms the count."""
+    without; HGRN2 with 128 x 128 heads two (the tensor-core pass and the pass
+    that re-runs marked heads: a redo pass of the same kernel for bf16, the
+    step-by-step kernel for fp32), other head dims one.  The ncu launch list
+    in profiles/ confirms the count for the step."""
     if cfg.form == "rglru":
         return 1
     if cfg.form == "selective":
         return 2 if cfg.io == "bf16" else 1
-    return 2 if (cfg.io == "bf16" and cfg.head_dim == 128) else 1
+    return 2 if cfg.head_dim == 128 else 1
 
 
 def input_bytes(p) -> int:
@@ -614,7 +616,7 @@ def gpu_arm(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": args.io or "bf16",
         "data": "synthetic (seeded generators with the pages' layer distributions)",
         "config": {"workload": " + ".join(c.name for c in cfgs),
                    "l2": "inputs larger than L2 (129 MB) on every launch, no flush",
