@@ -235,6 +235,19 @@ def test_selective_work_stealing(lr, io, splits):
     check_sel(lr, p, io)
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_selective_deferred_shares(lr, io):
+    """A warm-up limit of 64 steps: most pieces' windows are longer, so their
+    shares are left to the second launch, which takes their carries by
+    look-back and corrects their outputs, while the few that fit (the fastest
+    channels' horizons, or pieces near the sequence start) warm up and can be
+    split by idle warps -- both kinds in one call."""
+    p = wl.selective_inputs(2, 3000, 128, seed=50, io=io, with_h0=True)
+    lr.lr_set_split_override(6)
+    lr.lr_set_selective_warmup(64)
+    check_sel(lr, p, io)
+
+
 def off_lattice(A_log, seed, channels=None, scale=0.05):
     """A_log moved off the multi-scale lattice A[n] = (n+1) A[0] (all channels,
     or only `channels`), so the kernel's warps holding them take the general
