@@ -44,9 +44,10 @@
 //              state it needs (a second issuer keeps this state-dependent MMA
 //              from queueing behind the front's work on the next chunk);
 //   front (8)  gates -> Lambda, m; V~, V~' and 2^(Lambda - m) for chunk c; the
-//              causal mask of P_c (runs up to a chunk ahead of the back).  Its
-//              per-element exp2 / log2 chains are the longest per-chunk work,
-//              so it gets two warps per scheduler;
+//              causal mask of P_c (runs up to a chunk ahead of the back).  In
+//              a whole chunk the per-step factors are running products of the
+//              gates, so a thread takes two exp2 and one log2 per chunk
+//              instead of one per step; two warps per scheduler;
 //   back (4)   state update S = 2^Lambda_C S + dS (fp32, in registers: thread j
 //              holds key column j of the 64 rows), its bf16 copy for the next
 //              OX, then the outputs of chunk c.
@@ -182,14 +183,23 @@ struct FrontEnv {
 
 // One virtual chunk [lo, hi) of chunk c by the front: V~, V~', the masked P,
 // 2^(Lambda - m), 2^(m - B0) and the decay 2^(B1 - B0), then the hand-over to
-// the MMA issuer and the back.  loc: this thread's cumulative log2 gates
-// (from the chunk start); B0, B1: Lambda before the virtual chunk and at its
-// last step.  WHOLE: the chunk is not split (lo = 0, hi = 64), so no step is
-// masked.  Returns false when a wait failed (every front thread then returns
-// false).
+// the MMA issuer and the back.  B0, B1: Lambda before the virtual chunk and at
+// its last step.  Returns false when a wait failed (every front thread then
+// returns false).
+//   WHOLE = false (a piece of a split chunk): a = this thread's cumulative
+//   log2 gates from the chunk start; the factors are exp2 of their
+//   differences, zero outside [lo, hi).
+//   WHOLE = true (lo = 0, hi = 64, nothing masked): a = the running products
+//   of this thread's gates (a[u] = g_tb ... g_tb+u), r = the products of the
+//   gates after each step (r[u] = g_tb+u+1 ... g_tb+15), off = Lambda before
+//   the thread's first step and qsum = log2 of its 16 gates' product.  Then
+//   2^(Lambda_t - m) = 2^(off - m) a[u] and 2^(m - Lambda_t) = 2^(m - off -
+//   qsum) r[u]: two exp2 per thread instead of one per step (no quarter of
+//   a whole chunk decays by more than 2^-40, so the products stay normal).
 template <bool SPLIT, bool WHOLE>
 __device__ __forceinline__ bool front_vc(const FrontEnv &x, int c, int j, int nvc, int lo, int hi,
-                                         const float (&loc)[FSTEPS], float B0, float B1, int &v) {
+                                         const float (&a)[FSTEPS], const float (&r)[FSTEPS], float off,
+                                         float qsum, float B0, float B1, int &v) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int f = tid - 32 * KW, fw = warp - KW;
     const int i = f & (RB - 1), qt = f / RB;
@@ -206,10 +216,14 @@ __device__ __forceinline__ bool front_vc(const FrontEnv &x, int c, int j, int nv
     // m = the mean of B0 and B1 keeps every factor within 2^(+-spread/2)
     const float m = 0.5f * (B0 + B1);
     float *e1 = E1 + bi * (C * RB);
+    const float ea = WHOLE ? ex2_approx(off - m) : 0.0f, eb = WHOLE ? ex2_approx(m - off - qsum) : 0.0f;
 #pragma unroll
     for (int u = 0; u < FSTEPS; ++u) {
         const int t = tb + u;
-        e1[e1_index(t, i)] = (WHOLE || (t >= lo && t < hi)) ? ex2_approx(loc[u] - m) : 0.0f;
+        if (WHOLE)
+            e1[e1_index(t, i)] = ea * a[u];
+        else
+            e1[e1_index(t, i)] = (t >= lo && t < hi) ? ex2_approx(a[u] - m) : 0.0f;
     }
     if (WHOLE ? qt == 0 : qt == lo / FSTEPS) {
         EM[bi * RB + i] = ex2_approx(m - B0);
@@ -222,11 +236,15 @@ __device__ __forceinline__ bool front_vc(const FrontEnv &x, int c, int j, int nv
 #pragma unroll
     for (int u = 0; u < FSTEPS; u += 2) {
         const int t = tb + u;
-        const float w0 = (WHOLE || (t >= lo && t < hi)) ? ex2_approx(m - loc[u]) * __bfloat162float(sV[t * RB + i])
-                                                        : 0.0f;
-        const float w1 = (WHOLE || (t + 1 >= lo && t + 1 < hi))
-                             ? ex2_approx(m - loc[u + 1]) * __bfloat162float(sV[(t + 1) * RB + i])
-                             : 0.0f;
+        float w0, w1;
+        if (WHOLE) {
+            w0 = eb * r[u] * __bfloat162float(sV[t * RB + i]);
+            w1 = eb * r[u + 1] * __bfloat162float(sV[(t + 1) * RB + i]);
+        } else {
+            w0 = (t >= lo && t < hi) ? ex2_approx(m - a[u]) * __bfloat162float(sV[t * RB + i]) : 0.0f;
+            w1 = (t + 1 >= lo && t + 1 < hi) ? ex2_approx(m - a[u + 1]) * __bfloat162float(sV[(t + 1) * RB + i])
+                                             : 0.0f;
+        }
         vt[u / 2] = pack_bf16(w0, w1);
         vtp[u / 2] = pack_bf16(w0 * cm, w1 * cm);
     }
@@ -373,7 +391,7 @@ __device__ __forceinline__ bool front_split_chunk(const FrontEnv &x, int c, int 
                 if (tb + u == hi - 1) B1 = loc[u];
             }
         }
-        if (!front_vc<true, false>(x, c, j, nvc, lo, hi, loc, B0, B1, v)) return false;
+        if (!front_vc<true, false>(x, c, j, nvc, lo, hi, loc, loc, 0.0f, 0.0f, B0, B1, v)) return false;
     }
     return true;
 }
@@ -585,18 +603,24 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             const __nv_bfloat16 *sG = reinterpret_cast<const __nv_bfloat16 *>(sm + st * STAGE_BYTES + OFF_G);
             const bool ok = hw(&full[st], (c / NST) & 1);   // inputs landed
 
-            // cumulative log2 gates over this thread's steps (steps past L: g = 1)
+            // running products of this thread's gates, forward and backward
+            // (steps past L: g = 1), and the log2 of their product
             const int t0 = c * C;
-            float loc[FSTEPS];
-            float acc = 0.0f;
+            float pf[FSTEPS], pr[FSTEPS], gq[FSTEPS];
+            float prod = 1.0f;
 #pragma unroll
             for (int u = 0; u < FSTEPS; ++u) {
                 const int t = tb + u;
                 float gv = __bfloat162float(sG[t * RB + i]);
                 if (PRE) gv = fmaf(1.0f - lb, rcp_approx(1.0f + ex2_approx(-gv * kLog2e)), lb);
-                acc += t0 + t < L ? lg2_approx(gv) : 0.0f;
-                loc[u] = acc;
+                gq[u] = t0 + t < L ? gv : 1.0f;
+                prod *= gq[u];
+                pf[u] = prod;
             }
+            pr[FSTEPS - 1] = 1.0f;
+#pragma unroll
+            for (int u = FSTEPS - 2; u >= 0; --u) pr[u] = pr[u + 1] * gq[u + 1];
+            const float acc = lg2_approx(prod);
             // a gate that is not a number (or infinite) leaves NaN or +inf here
             if (!(acc == acc) || acc == __int_as_float(0x7f800000)) status_report(sref, LR_ERR_RANGE);
             TOTF[qt * RB + i] = acc;
@@ -620,13 +644,11 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                 off += q < qt ? tq : 0.0f;
                 lc += tq;
             }
-#pragma unroll
-            for (int u = 0; u < FSTEPS; ++u) loc[u] += off;
             if (SPLIT && f == 0) {   // one virtual chunk: tell the OX issuer
                 NVC[c & 3] = 1;
                 arrive(&splitr[c & 1]);
             }
-            if (!hg::front_vc<SPLIT, true>(fx, c, 0, 1, 0, C, loc, 0.0f, lc, v)) break;
+            if (!hg::front_vc<SPLIT, true>(fx, c, 0, 1, 0, C, pf, pr, off, acc, 0.0f, lc, v)) break;
         }
     } else {  // ------------------------------------------------------------ back
         // key column j = tid of value rows rb*64 .. rb*64+63 of S[b, h].  The
