@@ -235,16 +235,27 @@ __global__ void __launch_bounds__(hf::NT, 1)
             }
         }
 
-        // gates: cumulative log2 over this thread's 16 steps
-        float loc[FS];
-        float acc = 0.0f;
+        // gates: running products over this thread's 16 steps, forward
+        // (pf[u] = g_0 .. g_u) and backward (pr[u] = g_u+1 .. g_15), and the
+        // log2 of their product.  A head whose quarter product falls below
+        // 2^-kQuarterSafe is re-run step by step, so on the heads kept the
+        // products stay normal and the per-step factors need no exp2 of their
+        // own: 2^(Lambda_t - m) = 2^(off - m) pf[u], 2^(m - Lambda_t) =
+        // 2^(m - off - acc) pr[u]
+        float pf[FS], pr[FS];
+        float prod = 1.0f;
 #pragma unroll
         for (int u = 0; u < FS; ++u) {
             float gg = gv[u];
             if (PRE) gg = t0 + fs0 + u < L ? fmaf(1.0f - lb, rcp_approx(1.0f + ex2_approx(-gg * kLog2e)), lb) : 1.0f;
-            acc += lg2_approx(gg);
-            loc[u] = acc;
+            gv[u] = gg;
+            prod *= gg;
+            pf[u] = prod;
         }
+        pr[FS - 1] = 1.0f;
+#pragma unroll
+        for (int u = FS - 2; u >= 0; --u) pr[u] = pr[u + 1] * gv[u + 1];
+        const float acc = lg2_approx(prod);
         if (!(acc == acc) || acc == __int_as_float(0x7f800000)) status_report(sref, LR_ERR_RANGE);
         if (-acc > kQuarterSafe) flags[1] = 1;   // steep: the head is re-run step by step
         tot[fq * RB + fi] = acc;
@@ -273,12 +284,12 @@ __global__ void __launch_bounds__(hf::NT, 1)
             gc[fi] = ex2_approx(lc);
         }
         const float cm = ex2_approx(lc - m);
+        const float ea = ex2_approx(off - m), eb = ex2_approx(m - off - acc);
         float vt[FS], vtp[FS];
 #pragma unroll
         for (int u = 0; u < FS; ++u) {
-            const float lam = loc[u] + off;
-            e1[e1_index(fs0 + u, fi)] = ex2_approx(lam - m);
-            vt[u] = ex2_approx(m - lam) * vv[u];
+            e1[e1_index(fs0 + u, fi)] = ea * pf[u];
+            vt[u] = eb * pr[u] * vv[u];
             vtp[u] = vt[u] * cm;
         }
 #pragma unroll
