@@ -574,8 +574,9 @@ def gpu_arm(args):
     host_outs = [make_call(lr, c, p)() for c, p in zip(cfgs, host_inputs)]
     host_calls = [make_call(lr, c, p, out=o) for c, p, o in zip(cfgs, host_inputs, host_outs)]
     h2d = sum(input_bytes(p) for p in host_inputs)
-    for fn in host_calls:
-        fn()
+    for _ in range(max(1, args.warmup)):   # the same W warm-up steps as the device leg
+        for fn in host_calls:
+            fn()
     torch.cuda.synchronize()
     # every step returns with its outputs in the caller's host buffers (each
     # call synchronises); timed over up to 20 steps, per-step times kept
@@ -629,6 +630,7 @@ def gpu_arm(args):
                 "steps": e2e_steps, "ms_per_step": e2e_s * 1e3,
                 "ms_per_step_median": statistics.median(e2e_ms),
                 "ms_per_step_min": min(e2e_ms), "ms_per_step_max": max(e2e_ms),
+                "slowest_step": e2e_ms.index(max(e2e_ms)),
                 "path": "lr_*_fwd on pinned host buffers: the library copies each chunk in, "
                         "scans it and copies the outputs back (wall clock, host timer)"},
         "gpu_launches": sum(launches_per_call(c) for c in cfgs) * args.steps,
