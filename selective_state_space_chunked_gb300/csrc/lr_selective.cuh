@@ -68,7 +68,8 @@
 // loads, each feeding all the channels of a lane.
 //
 // Decays.  In general each state's decay is one exp2 of delta A[n] log2(e).
-// MultiScaleSSM.__init__ initialises A_log[d, n] = log((n+1) 2^s), so that
+// The cortexnet 3.2.1 ssm.py page (class MultiScaleSSM, its initialiser)
+// sets A_log[d, n] = log((n+1) 2^s), so that
 // A[n] = (n + 1) A[0]; on that lattice the 16 decays of a step are the powers
 // E, E^2, .., E^16 of E = exp(delta A[0]), taken as (E, E^2) from two exp2 and
 // the other pairs as P * (E^2, E^2).  Each warp checks the lattice itself from
