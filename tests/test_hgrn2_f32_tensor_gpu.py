@@ -85,6 +85,20 @@ def test_hgrn2_f32_steep_chunks_rerun_step_by_step(lr, kind):
     check(lr, p, 3, S0=0.1 * p["S0"])
 
 
+@pytest.mark.parametrize("e,rerun", [(-39.75, False), (-40.25, True)])
+def test_hgrn2_f32_gates_at_the_whole_chunk_limit(lr, e, rerun):
+    """Constant gates 2^(e/16) in one head: 16-step products just inside
+    (kept on the tensor cores, per-step factors from running products down to
+    2^-39.75) and just outside (the head is re-run step by step) the 2^-40
+    limit, beside ordinary gates in the other head, at the fp32 bar."""
+    p = f32_inputs(1, 320, 2, seed=78, with_S0=True)
+    g = p["g"].clone()
+    g[..., :128] = 2.0 ** (e / 16)
+    p["g"] = g
+    assert (16 * torch.log2(g[..., :128].double()) < -40).all().item() == rerun
+    check(lr, p, 2, S0=0.1 * p["S0"])
+
+
 @pytest.mark.parametrize("lb", [0.2, 0.0])
 def test_hgrn2_f32_tensor_preact(lr, lb):
     """Pre-activation gates, g = lb + (1 - lb) sigmoid(f), formed in the kernel."""

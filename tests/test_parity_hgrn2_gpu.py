@@ -133,6 +133,22 @@ def test_hgrn2_steep_chunk_in_one_block_only(lr):
     assert rel_err(o2.float().cpu(), orf) <= TOL and rel_err(S2.cpu(), Srf) <= TOL
 
 
+@pytest.mark.parametrize("gq,split", [(0.177734375, False), (0.17578125, True)])
+def test_hgrn2_gates_at_the_whole_chunk_limit(lr, gq, split):
+    """Constant gates (exact in bf16) whose 16-step products sit just inside
+    (2^-39.875: the chunk runs whole, its per-step factors span 2^+-79.75 and
+    come from running products as small as 2^-39.875) and just outside
+    (2^-40.13: the first pass marks every block, the second splits each chunk
+    in two) the whole-chunk limit of 2^-40 per quarter, beside ordinary gates
+    in the other head."""
+    p = wl.hgrn2_inputs(1, 320, 2, 128, seed=16, with_S0=True)
+    g = p["g"].float()
+    g[..., :128] = gq
+    p["g"] = g.to(torch.bfloat16)
+    assert (16 * torch.log2(p["g"][..., :128].double()) < -40).all().item() == split
+    check(lr, p, S0=0.1 * p["S0"])
+
+
 def test_hgrn2_small_gates_preact_lower_bound_zero(lr):
     """The page's default configuration: lb = 0 on pre-activation gates."""
     p = wl.hgrn2_inputs(1, 320, 2, 128, seed=12)
