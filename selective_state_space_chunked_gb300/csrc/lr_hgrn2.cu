@@ -30,7 +30,7 @@
 //
 // A thread block owns 64 value rows of one (batch, head) (rows of S evolve
 // independently because diag(g) scales rows): grid = B * H * 2, one block per
-// SM (223,472 bytes of shared memory, all 512 TMEM columns).  Four tcgen05 MMAs per
+// SM (224,496 bytes of shared memory, all 512 TMEM columns).  Four tcgen05 MMAs per
 // chunk (bf16 operands in shared memory, fp32 accumulators in TMEM):
 //   P    = Q K^T       M=64  N=64 K=128  A = Q (K-major), B = K (K-major), TMA 128B-swizzled
 //   dS^T = K^T V~'     M=128 N=64 K=64   A = the same K tile read MN-major, B = V~' (K-major)
@@ -47,7 +47,9 @@
 //              causal mask of P_c (runs up to a chunk ahead of the back).  In
 //              a whole chunk the per-step factors are running products of the
 //              gates, so a thread takes two exp2 and one log2 per chunk
-//              instead of one per step; two warps per scheduler;
+//              instead of one per step.  One block barrier per chunk (the
+//              exchange of quarter totals); each warp hands its operands over
+//              with its own mbarrier arrival.  Two warps per scheduler;
 //   back (4)   state update S = 2^Lambda_C S + dS (fp32, in registers: thread j
 //              holds key column j of the 64 rows), its bf16 copy for the next
 //              OX, then the outputs of chunk c.
@@ -94,8 +96,8 @@ constexpr uint32_t OFF_SBT = OFF_VTP + 8192;       // bf16 state [128 j][64 i], 
 constexpr uint32_t OFF_E1 = OFF_SBT + 16384;       // 2 x 2^(Lambda - m), fp32 [64 t][64 i]
 constexpr uint32_t OFF_EM = OFF_E1 + 2 * 16384;    // 2 x 2^m [64]
 constexpr uint32_t OFF_GC = OFF_EM + 2 * 256;      // 2 x 2^Lambda_C [64]
-constexpr uint32_t OFF_TOT = OFF_GC + 2 * 256;     // front: per-quarter totals [FQ][64]
-constexpr uint32_t OFF_VI = OFF_TOT + FQ * 256;    // 2 x virtual chunk (chunk, lo, hi, last)
+constexpr uint32_t OFF_TOT = OFF_GC + 2 * 256;     // front: per-quarter totals [2][FQ][64] (by chunk parity)
+constexpr uint32_t OFF_VI = OFF_TOT + 2 * FQ * 256;    // 2 x virtual chunk (chunk, lo, hi, last)
 constexpr uint32_t OFF_SPL = OFF_VI + 32;          // front: split flags of the chunk; [4..7]
                                                    // virtual chunks of chunk c % 4
 constexpr uint32_t OFF_BAR = OFF_SPL + 32;
@@ -286,17 +288,21 @@ __device__ __forceinline__ bool front_vc(const FrontEnv &x, int c, int j, int nv
             *reinterpret_cast<uint4 *>(Ps + t * 128 + ((chunk ^ (t & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
     }
+    // each front warp hands over on its own: the MMA issuer and the back wait
+    // for all eight arrivals (no block barrier, so a warp that is done goes on
+    // to the next chunk's gates); ok is uniform over the warp
     fence_proxy_async_smem();
     tc_fence_before();
-    if (named_bar_or(2, 32 * FW, !ok)) return false;
-    if (f == 0) {
-        const bool last = j == nvc - 1;
-        if (SPLIT) {
-            x.VI[4 * bi] = c;
-            x.VI[4 * bi + 1] = lo;
-            x.VI[4 * bi + 2] = hi;
-            x.VI[4 * bi + 3] = last ? 1 : 0;
-        }
+    if (!ok) return false;
+    const bool last = j == nvc - 1;
+    if (SPLIT && f == 0) {
+        x.VI[4 * bi] = c;
+        x.VI[4 * bi + 1] = lo;
+        x.VI[4 * bi + 2] = hi;
+        x.VI[4 * bi + 3] = last ? 1 : 0;
+    }
+    __syncwarp();
+    if (lane == 0) {
         arrive(&x.fdone[bi]);
         if (last) arrive(&x.empty[st]);   // V, g of stage st no longer read
     }
@@ -451,13 +457,13 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 3);   // the two MMA issuers' commits and the front
+            mbar_init(&empty[s], 2 + FW);   // the two MMA issuers' commits and each front warp
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&bar_p[k], 1);
             mbar_init(&bar_o[k], 1);
             mbar_init(&bar_x[k], 1);
-            mbar_init(&fdone[k], 1);
+            mbar_init(&fdone[k], FW);   // each front warp
             mbar_init(&kdone[k], KW);
         }
         mbar_init(sbready, KW);   // each back warp publishes its own 32 rows
@@ -623,7 +629,9 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             const float acc = lg2_approx(prod);
             // a gate that is not a number (or infinite) leaves NaN or +inf here
             if (!(acc == acc) || acc == __int_as_float(0x7f800000)) status_report(sref, LR_ERR_RANGE);
-            TOTF[qt * RB + i] = acc;
+            float *tot = TOTF + (c & 1) * (FQ * RB);   // by chunk parity: a warp ahead may
+                                                        // write the next chunk's totals
+            tot[qt * RB + i] = acc;
             // the quarter totals are exchanged here.  The barrier also ORs the
             // local test that rules out a split (this quarter's |sum of log2 g|
             // within kQuarterSafe) with a failed wait; only when it fires do
@@ -640,7 +648,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             float off = 0.0f, lc = 0.0f;
 #pragma unroll
             for (int q = 0; q < FQ; ++q) {
-                const float tq = TOTF[q * RB + i];
+                const float tq = tot[q * RB + i];
                 off += q < qt ? tq : 0.0f;
                 lc += tq;
             }
