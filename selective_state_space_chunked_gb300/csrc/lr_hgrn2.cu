@@ -101,8 +101,8 @@ constexpr uint32_t OFF_VI = OFF_TOT + 2 * FQ * 256;    // 2 x virtual chunk (chu
 constexpr uint32_t OFF_SPL = OFF_VI + 32;          // front: split flags of the chunk; [4..7]
                                                    // virtual chunks of chunk c % 4
 constexpr uint32_t OFF_BAR = OFF_SPL + 32;
-// full[3] empty[3] bar_p[2] bar_o[2] bar_x[2] fdone[2] kdone[2] sbready mma_done splitr[2]
-constexpr int NBAR = 3 + 3 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 2;
+// full[3] empty[3] bar_p[2] bar_o[2] bar_x[2] fdone[2] kdone[2] sbready mma_done splitr[2] bar_ds[2]
+constexpr int NBAR = 3 + 3 + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2;
 // the local test that rules out a split: every quarter (16 steps) of every
 // row within a quarter of the limit
 constexpr float kQuarterSafe = kMaxSpread / 4;
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *full = bars, *empty = bars + 3, *bar_p = bars + 6, *bar_o = bars + 8,
              *bar_x = bars + 10, *fdone = bars + 12, *kdone = bars + 14, *sbready = bars + 16,
-             *mma_done = bars + 17, *splitr = bars + 18;
+             *mma_done = bars + 17, *splitr = bars + 18, *bar_ds = bars + 20;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + OFF_FLAG);
     float *E1 = reinterpret_cast<float *>(sm + OFF_E1);
@@ -470,6 +470,8 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
         mbar_init(mma_done, 2);
         mbar_init(&splitr[0], 1);
         mbar_init(&splitr[1], 1);
+        mbar_init(&bar_ds[0], 1);
+        mbar_init(&bar_ds[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -544,6 +546,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                 for (int kk = 0; kk < C / 16; ++kk)
                     umma_bf16(tmem + T_DS + bi * 64, umma_smem_desc(sK + kk * 2048, 8192, 1024),
                               umma_smem_desc(smem_u32(VTP) + kk * 32, 16, 1024), IDESC_DS, kk > 0);
+                umma_commit(&bar_ds[bi]);   // the back's state update need not wait for OI
 #pragma unroll
                 for (int kk = 0; kk < C / 16; ++kk)
                     umma_bf16(tmem + T_OI + bi * 64, umma_smem_desc(smem_u32(Ps) + kk * 32, 16, 1024),
@@ -689,7 +692,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
         for (int c = 0, v = 0; c < n_chunks; ++v) {
             const int bi = v & 1;
             bool ok = hw(&fdone[bi], (v >> 1) & 1);
-            if (ok) ok = hw(&bar_o[bi], (v >> 1) & 1);
+            if (ok) ok = hw(&bar_ds[bi], (v >> 1) & 1);
             if (!__all_sync(FULLM, ok)) break;
             const int lo = SPLIT ? VI[4 * bi + 1] : 0, hi = SPLIT ? VI[4 * bi + 2] : C;
             const bool last = !SPLIT || VI[4 * bi + 3] != 0;
@@ -718,8 +721,9 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                     }
                 }
             }
-            // OX_v reads the previous bf16 state until bar_x
-            ok = hw(&bar_x[bi], (v >> 1) & 1);
+            // OI_v, and OX_v, which reads the previous bf16 state until bar_x
+            ok = hw(&bar_o[bi], (v >> 1) & 1);
+            if (ok) ok = hw(&bar_x[bi], (v >> 1) & 1);
             if (!__all_sync(FULLM, ok)) break;
             tc_fence_after();
             // the first output columns' accumulator loads overlap the state write
