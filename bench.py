@@ -579,8 +579,8 @@ def gpu_arm(args):
             fn()
     torch.cuda.synchronize()
     # every step returns with its outputs in the caller's host buffers (each
-    # call synchronises); timed over up to 20 steps, per-step times kept
-    e2e_steps = max(3, min(args.steps, 20))
+    # call synchronises); timed over up to 50 steps, per-step times kept
+    e2e_steps = max(3, min(args.steps, 50))
     barrier(world)
     d2h = 0
     e2e_ms = []
