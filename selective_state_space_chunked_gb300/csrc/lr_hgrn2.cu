@@ -186,8 +186,8 @@ struct FrontEnv {
 // One virtual chunk [lo, hi) of chunk c by the front: V~, V~', the masked P,
 // 2^(Lambda - m), 2^(m - B0) and the decay 2^(B1 - B0), then the hand-over to
 // the MMA issuer and the back.  B0, B1: Lambda before the virtual chunk and at
-// its last step.  Returns false when a wait failed (every front thread then
-// returns false).
+// its last step.  Returns false, for the whole warp, when one of its waits
+// failed; the warp then skips its hand-over.
 //   WHOLE = false (a piece of a split chunk): a = this thread's cumulative
 //   log2 gates from the chunk start; the factors are exp2 of their
 //   differences, zero outside [lo, hi).
@@ -607,10 +607,15 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
         const hg::FrontEnv fx{sm, tmem, empty, bar_p, bar_o, fdone, kdone, splitr, abort_flag, VI, NVC,
                               L, lb, timeout_ns, sref};
         int v = 0;   // virtual chunks so far
+        // a wait of this warp ran out (or saw the abort flag) in an earlier
+        // chunk's hand-over: the warp carries that to the next quarter-total
+        // exchange, where all front warps leave the loop together (a warp that
+        // left alone would leave the others at that barrier)
+        bool failed = false;
         for (int c = 0; c < n_chunks; ++c) {
             const int st = c % NST;
             const __nv_bfloat16 *sG = reinterpret_cast<const __nv_bfloat16 *>(sm + st * STAGE_BYTES + OFF_G);
-            const bool ok = hw(&full[st], (c / NST) & 1);   // inputs landed
+            const bool ok = !failed && hw(&full[st], (c / NST) & 1);   // inputs landed
 
             // running products of this thread's gates, forward and backward
             // (steps past L: g = 1), and the log2 of their product
@@ -642,7 +647,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
             if (named_bar_or(2, 32 * FW, !ok || -acc > kQuarterSafe)) {
                 if (named_bar_or(3, 32 * FW, !ok)) break;
                 if constexpr (SPLIT) {
-                    if (!hg::front_split_chunk<PRE>(fx, c, v)) break;
+                    if (!hg::front_split_chunk<PRE>(fx, c, v)) failed = true;
                     continue;
                 } else {
                     if (f == 0) redo[blockIdx.x] = sref.stamp;   // the second pass redoes this block
@@ -659,7 +664,7 @@ __global__ void __launch_bounds__(hg::THREADS, 1)
                 NVC[c & 3] = 1;
                 arrive(&splitr[c & 1]);
             }
-            if (!hg::front_vc<SPLIT, true>(fx, c, 0, 1, 0, C, pf, pr, off, acc, 0.0f, lc, v)) break;
+            if (!hg::front_vc<SPLIT, true>(fx, c, 0, 1, 0, C, pf, pr, off, acc, 0.0f, lc, v)) failed = true;
         }
     } else {  // ------------------------------------------------------------ back
         // key column j = tid of value rows rb*64 .. rb*64+63 of S[b, h].  The
