@@ -30,7 +30,7 @@
 //
 // A thread block owns 64 value rows of one (batch, head) (rows of S evolve
 // independently because diag(g) scales rows): grid = B * H * 2, one block per
-// SM (224,496 bytes of shared memory, all 512 TMEM columns).  Four tcgen05 MMAs per
+// SM (224,512 bytes of shared memory, all 512 TMEM columns).  Four tcgen05 MMAs per
 // chunk (bf16 operands in shared memory, fp32 accumulators in TMEM):
 //   P    = Q K^T       M=64  N=64 K=128  A = Q (K-major), B = K (K-major), TMA 128B-swizzled
 //   dS^T = K^T V~'     M=128 N=64 K=64   A = the same K tile read MN-major, B = V~' (K-major)
