@@ -297,18 +297,31 @@ def cpu_baseline(cfgs, repeats=1, samples=None, single_thread=False) -> dict:
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
-def make_call(lr, cfg, p, out=None, ws=None):
+def make_call(lr, cfg, p, out=None, ws=None, sync_host=True):
     """One call of a workload's scan through the public torch API; ``ws``: the
     workspace tensor it keeps using (its first bytes hold each call's device
-    status)."""
+    status); ``sync_host=False``: a host-buffer call returns once queued."""
     if cfg.form == "rglru":
         return lambda: lr.rglru_scan(p["x"], p["r"], p["i"], p["a_log"], p["c"], h0=p["h0"],
-                                     out=out, workspace=ws)
+                                     out=out, workspace=ws, sync_host=sync_host)
     if cfg.form == "selective":
         return lambda: lr.selective_scan(p["x"], p["dt"], p["Bm"], p["Cm"], p["A_log"],
                                          z=p["z"], Dskip=p["Dskip"], h0=p["h0"], out=out,
-                                         workspace=ws)
-    return lambda: lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=p["H"], out=out, workspace=ws)
+                                         workspace=ws, sync_host=sync_host)
+    return lambda: lr.hgrn2(p["q"], p["k"], p["v"], p["g"], H=p["H"], out=out, workspace=ws,
+                            sync_host=sync_host)
+
+
+def host_workspace_for(lr, cfg, dev):
+    """The device staging workspace of one workload's host-buffer call."""
+    io = lr.LR_BF16 if cfg.io == "bf16" else lr.LR_F32
+    if cfg.form == "rglru":
+        n = lr.lr_rglru_scan_fwd_host_workspace_size(cfg.B, cfg.L, cfg.D, io)
+    elif cfg.form == "selective":
+        n = lr.lr_selective_scan_fwd_host_workspace_size(cfg.B, cfg.L, cfg.D, cfg.N, io)
+    else:
+        n = lr.lr_hgrn2_fwd_host_workspace_size(cfg.B, cfg.L, cfg.H, cfg.head_dim, cfg.head_dim, io)
+    return torch.empty(max(int(n), 256), dtype=torch.uint8, device=dev)
 
 
 def workspace_for(lr, cfg, dev):
@@ -570,16 +583,22 @@ def gpu_arm(args):
     # the library copies them in, runs, copies outputs back and synchronises
     host_inputs = [{k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in p.items()}
                    for p in inputs]
-    # the caller's result buffers: pinned host tensors, allocated once
+    # the caller's result buffers: pinned host tensors, allocated once; each
+    # scan has its own staging workspace, so its queued calls can overlap
     host_outs = [make_call(lr, c, p)() for c, p in zip(cfgs, host_inputs)]
-    host_calls = [make_call(lr, c, p, out=o) for c, p, o in zip(cfgs, host_inputs, host_outs)]
+    host_wss = [host_workspace_for(lr, c, dev) for c in cfgs]
+    host_calls = [make_call(lr, c, p, out=o, ws=w, sync_host=False)
+                  for c, p, o, w in zip(cfgs, host_inputs, host_outs, host_wss)]
     h2d = sum(input_bytes(p) for p in host_inputs)
     for _ in range(max(1, args.warmup)):   # the same W warm-up steps as the device leg
         for fn in host_calls:
             fn()
+        lr.host_sync()
     torch.cuda.synchronize()
-    # every step returns with its outputs in the caller's host buffers (each
-    # call synchronises); timed over up to 50 steps, per-step times kept
+    # every step queues the three scans' host-buffer calls (each returns once
+    # its work is queued, so one call's inputs go in while the previous one's
+    # last chunks run) and returns when lr.host_sync() has every output in the
+    # caller's host buffers; timed over up to 50 steps, per-step times kept
     e2e_steps = max(3, min(args.steps, 50))
     barrier(world)
     d2h = 0
@@ -591,10 +610,12 @@ def gpu_arm(args):
         for fn in host_calls:
             outs = fn()
             d2h += sum(t.numel() * t.element_size() for t in outs)
+        lr.host_sync()
         e2e_ms.append((time.perf_counter() - ts) * 1e3)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev) / e2e_steps
-    del host_inputs, host_calls, host_outs
+    check_calls(lr, host_wss, stream, "in the end-to-end leg")
+    del host_inputs, host_calls, host_outs, host_wss
 
     units_step = sum(a["units"] for a in alg)
     value = job_throughput(world, units_step, args.steps, total_ms)
@@ -631,8 +652,9 @@ def gpu_arm(args):
                 "ms_per_step_median": statistics.median(e2e_ms),
                 "ms_per_step_min": min(e2e_ms), "ms_per_step_max": max(e2e_ms),
                 "slowest_step": e2e_ms.index(max(e2e_ms)),
-                "path": "lr_*_fwd on pinned host buffers: the library copies each chunk in, "
-                        "scans it and copies the outputs back (wall clock, host timer)"},
+                "path": "lr_*_fwd_host_async on pinned host buffers, one lr_host_sync per step: the "
+                        "library copies each chunk in, scans it and copies the outputs back, the "
+                        "three calls overlapping (wall clock, host timer)"},
         "gpu_launches": sum(launches_per_call(c) for c in cfgs) * args.steps,
         "clocks": clk,
     }

@@ -349,7 +349,8 @@ int lr_minmax_scan_fwd(const void *r, const void *s, const float *x0, void *y,
  *     the device call's own workspace).  The size covers the optional
  *     tensors (z, Dskip) whether or not a call passes them.
  *   - Calls on one device run one after another (the library's streams are
- *     shared; a mutex serialises them).
+ *     shared; a mutex serialises them).  The *_async forms below queue the
+ *     same work and return without waiting for it.
  */
 size_t lr_selective_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D,
                                                  int64_t N, lr_dtype io);
@@ -383,6 +384,56 @@ int lr_minmax_scan_fwd_host(const void *r, const void *s, const float *x0, void 
                             float *x_final, int64_t B, int64_t L, int64_t D,
                             lr_dtype io, void *workspace, size_t ws_bytes,
                             lr_stream_t stream);
+
+/*
+ * Asynchronous forms of the four host-buffer calls (a library facility; the
+ * pages specify only the recurrences).  Same arguments, checks and results
+ * as the synchronous forms, but each returns once its chunks are queued on
+ * the library's streams, so consecutive calls overlap: the next call's
+ * inputs go in while this call's last chunks run and its outputs come out.
+ *   - Every host buffer of the call stays in use (inputs read, outputs and
+ *     the final state written) until lr_host_sync() returns: the caller keeps
+ *     them allocated and unchanged and reads no result before then.
+ *   - Each call in flight needs a workspace of its own (two calls sharing one
+ *     would overwrite each other's staging buffers); it too is in use until
+ *     lr_host_sync() returns.
+ *   - A call must not read a host buffer that an earlier call in flight
+ *     writes (running a sequence in segments through h_final -> h0 needs
+ *     lr_host_sync() between the segments).
+ *   - Errors found before anything is queued (arguments, workspace size)
+ *     are returned as by the synchronous form.  The device-side status of a
+ *     call (a bounded wait that ran out) is read after lr_host_sync() with
+ *     lr_check_status(workspace, stream).
+ * Calls on one device queue in call order (a mutex serialises the queueing).
+ */
+int lr_selective_scan_fwd_host_async(const void *x, const void *dt, const void *z,
+                                     const void *Bm, const void *Cm,
+                                     const float *A_log, const float *Dskip,
+                                     const float *h0, void *y, float *h_final,
+                                     int64_t B, int64_t L, int64_t D, int64_t N,
+                                     lr_dtype io, int dt_softplus,
+                                     void *workspace, size_t ws_bytes, lr_stream_t stream);
+int lr_rglru_scan_fwd_host_async(const void *x, const void *r, const void *i,
+                                 const float *a_log, float c, const float *h0,
+                                 void *y, float *h_final,
+                                 int64_t B, int64_t L, int64_t D, lr_dtype io,
+                                 void *workspace, size_t ws_bytes, lr_stream_t stream);
+int lr_hgrn2_fwd_host_async(const void *q, const void *k, const void *v, const void *g,
+                            const float *S0, void *o, float *S_final,
+                            int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
+                            int64_t chunk, lr_dtype io,
+                            void *workspace, size_t ws_bytes, lr_stream_t stream);
+int lr_minmax_scan_fwd_host_async(const void *r, const void *s, const float *x0, void *y,
+                                  float *x_final, int64_t B, int64_t L, int64_t D,
+                                  lr_dtype io, void *workspace, size_t ws_bytes,
+                                  lr_stream_t stream);
+
+/*
+ * Waits until every host-buffer call queued on the current device has
+ * finished (its outputs and final state are in host memory).  Returns LR_OK,
+ * or LR_ERR_CUDA when a CUDA call failed.
+ */
+int lr_host_sync(void);
 
 /* ------------------------------------------------------------------------ */
 /* Single-token decode steps                                                 */

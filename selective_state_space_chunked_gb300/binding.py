@@ -74,6 +74,14 @@ SIGNATURES = {
                                _I64, _I64, _I, _P, _SZ, _P]),
     "lr_minmax_scan_fwd_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
     "lr_minmax_scan_fwd_host": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_selective_scan_fwd_host_async": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                              _I64, _I64, _I64, _I64, _I, _I, _P, _SZ, _P]),
+    "lr_rglru_scan_fwd_host_async": (_I, [_P, _P, _P, _P, _F, _P, _P, _P,
+                                          _I64, _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_hgrn2_fwd_host_async": (_I, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                     _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_minmax_scan_fwd_host_async": (_I, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I, _P, _SZ, _P]),
+    "lr_host_sync": (_I, []),
 }
 
 
@@ -264,6 +272,39 @@ def lr_minmax_scan_fwd_host(r, s, x0, y, x_final, B, L, D, io, workspace, ws_byt
                                             stream))
 
 
+def lr_selective_scan_fwd_host_async(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, N, io,
+                                     dt_softplus, workspace, ws_bytes, stream) -> int:
+    """As lr_selective_scan_fwd_host, returning once the work is queued."""
+    return int(_lib.lr_selective_scan_fwd_host_async(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final,
+                                                     B, L, D, N, io, dt_softplus, workspace, ws_bytes,
+                                                     stream))
+
+
+def lr_rglru_scan_fwd_host_async(x, r, i, a_log, c, h0, y, h_final, B, L, D, io, workspace, ws_bytes,
+                                 stream) -> int:
+    """As lr_rglru_scan_fwd_host, returning once the work is queued."""
+    return int(_lib.lr_rglru_scan_fwd_host_async(x, r, i, a_log, c, h0, y, h_final, B, L, D, io,
+                                                 workspace, ws_bytes, stream))
+
+
+def lr_hgrn2_fwd_host_async(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io, workspace, ws_bytes,
+                            stream) -> int:
+    """As lr_hgrn2_fwd_host, returning once the work is queued."""
+    return int(_lib.lr_hgrn2_fwd_host_async(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io,
+                                            workspace, ws_bytes, stream))
+
+
+def lr_minmax_scan_fwd_host_async(r, s, x0, y, x_final, B, L, D, io, workspace, ws_bytes, stream) -> int:
+    """As lr_minmax_scan_fwd_host, returning once the work is queued."""
+    return int(_lib.lr_minmax_scan_fwd_host_async(r, s, x0, y, x_final, B, L, D, io, workspace, ws_bytes,
+                                                  stream))
+
+
+def lr_host_sync() -> int:
+    """Waits for every host-buffer call queued on the current device."""
+    return int(_lib.lr_host_sync())
+
+
 # ------------------------------------------------------------ torch helpers
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
@@ -414,6 +455,46 @@ def _host_workspace(nbytes: int, given: Optional[torch.Tensor]):
     return ws, nbytes
 
 
+# tensors that host-buffer calls queued with sync_host=False still read or
+# write (inputs, results, workspaces), per device, until host_sync()
+_ASYNC_KEEP = {}
+
+
+def _async_workspace(nbytes: int, given: Optional[torch.Tensor]):
+    """Device staging for a queued host-buffer call: the caller's tensor, or a
+    new one (calls in flight must not share one)."""
+    if nbytes == (1 << 64) - 1:
+        raise LrError(LR_ERR_CUDA, "workspace size query")
+    if nbytes == 0:
+        return None, 0
+    if given is not None:
+        _tls.ws = given
+        return given, given.numel() * given.element_size()
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=torch.device("cuda", torch.cuda.current_device()))
+    _tls.ws = ws
+    return ws, nbytes
+
+
+def _host_entry(sync_fn, async_fn, nbytes, workspace, sync_host: bool, keep):
+    """The host-buffer entry point and its workspace: synchronous, or queued
+    (its tensors kept alive until host_sync())."""
+    if sync_host:
+        ws, wsb = _host_workspace(nbytes, workspace)
+        return sync_fn, ws, wsb
+    ws, wsb = _async_workspace(nbytes, workspace)
+    _ASYNC_KEEP.setdefault(torch.cuda.current_device(), []).extend(
+        [t for t in list(keep) + [ws] if t is not None])
+    return async_fn, ws, wsb
+
+
+def host_sync() -> None:
+    """Waits for every host-buffer call queued with ``sync_host=False`` on the
+    current device; their results are then in host memory (read each call's
+    device-side status afterwards with ``status(workspace)``)."""
+    _check(lr_host_sync(), "lr_host_sync")
+    _ASYNC_KEEP.pop(torch.cuda.current_device(), None)
+
+
 def _host_stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
@@ -440,7 +521,9 @@ def selective_scan(x, dt, Bm, Cm, A_log, z=None, Dskip=None, h0=None,
     host).  Host inputs with host (or no) ``out`` run the library's
     host-buffer path (chunked, copies overlapping the scan; pinned memory
     keeps the copies asynchronous); ``workspace`` is then its device
-    staging buffer."""
+    staging buffer.  With ``sync_host=False`` a host-buffer call returns once
+    its work is queued, so consecutive calls overlap; ``host_sync()`` waits
+    for it (each queued call without a ``workspace`` gets a new one)."""
     if _host_route((x, dt, z, Bm, Cm), out):
         x, dt, z, Bm, Cm = (_h(t) for t in (x, dt, z, Bm, Cm))
         A_log, Dskip, h0 = (_h(t, torch.float32) for t in (A_log, Dskip, h0))
@@ -449,11 +532,12 @@ def selective_scan(x, dt, Bm, Cm, A_log, z=None, Dskip=None, h0=None,
         B, L, D = x.shape
         N = Bm.shape[-1]
         y, hf = _host_outputs(out, [((B, L, D), x.dtype), ((B, D, N), torch.float32)])
-        ws, wsb = _host_workspace(lr_selective_scan_fwd_host_workspace_size(B, L, D, N, io), workspace)
-        _check(lr_selective_scan_fwd_host(_ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _ptr(A_log),
-                                          _ptr(Dskip), _ptr(h0), _ptr(y), _ptr(hf), B, L, D, N, io,
-                                          int(bool(dt_softplus)), _ptr(ws), wsb, _host_stream()),
-               "lr_selective_scan_fwd_host")
+        fn, ws, wsb = _host_entry(lr_selective_scan_fwd_host, lr_selective_scan_fwd_host_async,
+                                  lr_selective_scan_fwd_host_workspace_size(B, L, D, N, io), workspace,
+                                  sync_host, (x, dt, z, Bm, Cm, A_log, Dskip, h0, y, hf))
+        _check(fn(_ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _ptr(A_log), _ptr(Dskip), _ptr(h0),
+                  _ptr(y), _ptr(hf), B, L, D, N, io, int(bool(dt_softplus)), _ptr(ws), wsb,
+                  _host_stream()), fn.__name__)
         return y, hf
     host = x.device.type != "cuda"
     dev = _target_device(x)
@@ -480,7 +564,8 @@ def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None, out=None
     a_log: (D,) fp32; h0: (B, D) fp32.  Returns (y (B, L, D), h_final (B, D)
     fp32); ``out=(y, h_final)`` gives the result tensors (GPU or host).  Host
     inputs with host (or no) ``out`` run the library's host-buffer path
-    (activated gates only)."""
+    (activated gates only; ``sync_host=False`` queues it, as for
+    ``selective_scan``)."""
     if not gates_preact and _host_route((x, r, i), out):
         x, r, i = (_h(t) for t in (x, r, i))
         a_log, h0 = (_h(t, torch.float32) for t in (a_log, h0))
@@ -488,10 +573,11 @@ def rglru_scan(x, r, i, a_log, c: float = 8.0, h0=None, workspace=None, out=None
         io = _io_of(x)
         B, L, D = x.shape
         y, hf = _host_outputs(out, [((B, L, D), x.dtype), ((B, D), torch.float32)])
-        ws, wsb = _host_workspace(lr_rglru_scan_fwd_host_workspace_size(B, L, D, io), workspace)
-        _check(lr_rglru_scan_fwd_host(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c), _ptr(h0),
-                                      _ptr(y), _ptr(hf), B, L, D, io, _ptr(ws), wsb, _host_stream()),
-               "lr_rglru_scan_fwd_host")
+        fn, ws, wsb = _host_entry(lr_rglru_scan_fwd_host, lr_rglru_scan_fwd_host_async,
+                                  lr_rglru_scan_fwd_host_workspace_size(B, L, D, io), workspace, sync_host,
+                                  (x, r, i, a_log, h0, y, hf))
+        _check(fn(_ptr(x), _ptr(r), _ptr(i), _ptr(a_log), float(c), _ptr(h0), _ptr(y), _ptr(hf),
+                  B, L, D, io, _ptr(ws), wsb, _host_stream()), fn.__name__)
         return y, hf
     host = x.device.type != "cuda"
     dev = _target_device(x)
@@ -517,8 +603,9 @@ def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None
     dtype (bfloat16 or float32); S0: (B, H, dv, dk) fp32.  Returns (o (B, L, H*dv), S_final
     (B, H, dv, dk) fp32); ``out=(o, S_final)`` gives the result tensors (GPU
     or host).  Host inputs with host (or no) ``out`` run the library's
-    host-buffer path (activated gates only).  Raises ValueError when the
-    hidden size is not divisible by the head count."""
+    host-buffer path (activated gates only; ``sync_host=False`` queues it, as
+    for ``selective_scan``).  Raises ValueError when the hidden size is not
+    divisible by the head count."""
     if q.shape[-1] % H or v.shape[-1] % H:
         raise ValueError(f"hidden size {q.shape[-1]} is not divisible by {H} heads")
     if gate_lb is None and _host_route((q, k, v, g), out):
@@ -529,10 +616,11 @@ def hgrn2(q, k, v, g, H: int, S0=None, chunk: int = 64, workspace=None, out=None
         B, L, HK = q.shape
         dk, dv = HK // H, v.shape[-1] // H
         o, Sf = _host_outputs(out, [((B, L, H * dv), q.dtype), ((B, H, dv, dk), torch.float32)])
-        ws, wsb = _host_workspace(lr_hgrn2_fwd_host_workspace_size(B, L, H, dk, dv, io), workspace)
-        _check(lr_hgrn2_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0), _ptr(o), _ptr(Sf),
-                                 B, L, H, dk, dv, chunk, io, _ptr(ws), wsb, _host_stream()),
-               "lr_hgrn2_fwd_host")
+        fn, ws, wsb = _host_entry(lr_hgrn2_fwd_host, lr_hgrn2_fwd_host_async,
+                                  lr_hgrn2_fwd_host_workspace_size(B, L, H, dk, dv, io), workspace, sync_host,
+                                  (q, k, v, g, S0, o, Sf))
+        _check(fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S0), _ptr(o), _ptr(Sf),
+                  B, L, H, dk, dv, chunk, io, _ptr(ws), wsb, _host_stream()), fn.__name__)
         return o, Sf
     host = q.device.type != "cuda"
     dev = _target_device(q)
@@ -563,7 +651,8 @@ def minmax_scan(r, s, x0=None, workspace=None, out=None,
     one dtype (float32 or bfloat16); x0: (B, D) fp32 or None (zero).
     Returns (y (B, L, D) = the state after every step, x_final (B, D) fp32);
     ``out=(y, x_final)`` gives the result tensors (GPU or host).  Host inputs
-    with host (or no) ``out`` run the library's host-buffer path."""
+    with host (or no) ``out`` run the library's host-buffer path
+    (``sync_host=False`` queues it, as for ``selective_scan``)."""
     if _host_route((r, s), out):
         r, s = (_h(t) for t in (r, s))
         x0 = _h(x0, torch.float32)
@@ -571,9 +660,11 @@ def minmax_scan(r, s, x0=None, workspace=None, out=None,
         io = _io_of(r)
         B, L, D = r.shape
         y, xf = _host_outputs(out, [((B, L, D), r.dtype), ((B, D), torch.float32)])
-        ws, wsb = _host_workspace(lr_minmax_scan_fwd_host_workspace_size(B, L, D, io), workspace)
-        _check(lr_minmax_scan_fwd_host(_ptr(r), _ptr(s), _ptr(x0), _ptr(y), _ptr(xf), B, L, D, io,
-                                       _ptr(ws), wsb, _host_stream()), "lr_minmax_scan_fwd_host")
+        fn, ws, wsb = _host_entry(lr_minmax_scan_fwd_host, lr_minmax_scan_fwd_host_async,
+                                  lr_minmax_scan_fwd_host_workspace_size(B, L, D, io), workspace, sync_host,
+                                  (r, s, x0, y, xf))
+        _check(fn(_ptr(r), _ptr(s), _ptr(x0), _ptr(y), _ptr(xf), B, L, D, io, _ptr(ws), wsb,
+                  _host_stream()), fn.__name__)
         return y, xf
     host = r.device.type != "cuda"
     dev = _target_device(r)

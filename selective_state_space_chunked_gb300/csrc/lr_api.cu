@@ -663,11 +663,10 @@ extern "C" size_t lr_selective_scan_fwd_host_workspace_size(int64_t B, int64_t L
     return j.kernel_ws == SIZE_MAX ? SIZE_MAX : lr::host_workspace_bytes(j);
 }
 
-extern "C" int lr_selective_scan_fwd_host(const void *x, const void *dt, const void *z, const void *Bm,
-                                          const void *Cm, const float *A_log, const float *Dskip,
-                                          const float *h0, void *y, float *h_final, int64_t B, int64_t L,
-                                          int64_t D, int64_t N, lr_dtype io, int dt_softplus,
-                                          void *workspace, size_t ws_bytes, lr_stream_t stream) {
+static int selective_host(const void *x, const void *dt, const void *z, const void *Bm, const void *Cm,
+                          const float *A_log, const float *Dskip, const float *h0, void *y, float *h_final,
+                          int64_t B, int64_t L, int64_t D, int64_t N, lr_dtype io, int dt_softplus,
+                          void *workspace, size_t ws_bytes, lr_stream_t stream, bool async_) {
     int rc = validate_selective(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, N, io);
     if (rc != LR_OK) return rc;
     if (B == 0 || D == 0) return LR_OK;
@@ -678,7 +677,25 @@ extern "C" int lr_selective_scan_fwd_host(const void *x, const void *dt, const v
     const SelHost a{B, D, N, io, dt_softplus, z != nullptr};
     const lr::HostJob j = sel_host_job(a, L, x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, Dskip != nullptr);
     if ((rc = host_ws_check(j, workspace, ws_bytes)) != LR_OK) return rc;
-    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), async_);
+}
+
+extern "C" int lr_selective_scan_fwd_host(const void *x, const void *dt, const void *z, const void *Bm,
+                                          const void *Cm, const float *A_log, const float *Dskip,
+                                          const float *h0, void *y, float *h_final, int64_t B, int64_t L,
+                                          int64_t D, int64_t N, lr_dtype io, int dt_softplus, void *workspace,
+                                          size_t ws_bytes, lr_stream_t stream) {
+    return selective_host(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, N, io, dt_softplus,
+                          workspace, ws_bytes, stream, false);
+}
+
+extern "C" int lr_selective_scan_fwd_host_async(const void *x, const void *dt, const void *z, const void *Bm,
+                                                const void *Cm, const float *A_log, const float *Dskip,
+                                                const float *h0, void *y, float *h_final, int64_t B,
+                                                int64_t L, int64_t D, int64_t N, lr_dtype io, int dt_softplus,
+                                                void *workspace, size_t ws_bytes, lr_stream_t stream) {
+    return selective_host(x, dt, z, Bm, Cm, A_log, Dskip, h0, y, h_final, B, L, D, N, io, dt_softplus,
+                          workspace, ws_bytes, stream, true);
 }
 
 extern "C" size_t lr_rglru_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io) {
@@ -688,10 +705,9 @@ extern "C" size_t lr_rglru_scan_fwd_host_workspace_size(int64_t B, int64_t L, in
     return j.kernel_ws == SIZE_MAX ? SIZE_MAX : lr::host_workspace_bytes(j);
 }
 
-extern "C" int lr_rglru_scan_fwd_host(const void *x, const void *r, const void *i, const float *a_log, float c,
-                                      const float *h0, void *y, float *h_final, int64_t B, int64_t L,
-                                      int64_t D, lr_dtype io, void *workspace, size_t ws_bytes,
-                                      lr_stream_t stream) {
+static int rglru_host(const void *x, const void *r, const void *i, const float *a_log, float c,
+                      const float *h0, void *y, float *h_final, int64_t B, int64_t L, int64_t D, lr_dtype io,
+                      void *workspace, size_t ws_bytes, lr_stream_t stream, bool async_) {
     int rc = validate_rglru(x, r, i, a_log, c, h0, y, h_final, B, L, D, io);
     if (rc != LR_OK) return rc;
     if (B == 0 || D == 0) return LR_OK;
@@ -702,7 +718,21 @@ extern "C" int lr_rglru_scan_fwd_host(const void *x, const void *r, const void *
     const RgHost a{B, D, io, c};
     const lr::HostJob j = rg_host_job(a, L, x, r, i, a_log, h0, y, h_final);
     if ((rc = host_ws_check(j, workspace, ws_bytes)) != LR_OK) return rc;
-    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), async_);
+}
+
+extern "C" int lr_rglru_scan_fwd_host(const void *x, const void *r, const void *i, const float *a_log,
+                                      float c, const float *h0, void *y, float *h_final, int64_t B, int64_t L,
+                                      int64_t D, lr_dtype io, void *workspace, size_t ws_bytes,
+                                      lr_stream_t stream) {
+    return rglru_host(x, r, i, a_log, c, h0, y, h_final, B, L, D, io, workspace, ws_bytes, stream, false);
+}
+
+extern "C" int lr_rglru_scan_fwd_host_async(const void *x, const void *r, const void *i, const float *a_log,
+                                            float c, const float *h0, void *y, float *h_final, int64_t B,
+                                            int64_t L, int64_t D, lr_dtype io, void *workspace,
+                                            size_t ws_bytes, lr_stream_t stream) {
+    return rglru_host(x, r, i, a_log, c, h0, y, h_final, B, L, D, io, workspace, ws_bytes, stream, true);
 }
 
 extern "C" size_t lr_hgrn2_fwd_host_workspace_size(int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv,
@@ -713,10 +743,9 @@ extern "C" size_t lr_hgrn2_fwd_host_workspace_size(int64_t B, int64_t L, int64_t
     return j.kernel_ws == SIZE_MAX ? SIZE_MAX : lr::host_workspace_bytes(j);
 }
 
-extern "C" int lr_hgrn2_fwd_host(const void *q, const void *k, const void *v, const void *g, const float *S0,
-                                 void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
-                                 int64_t dv, int64_t chunk, lr_dtype io, void *workspace, size_t ws_bytes,
-                                 lr_stream_t stream) {
+static int hgrn2_host(const void *q, const void *k, const void *v, const void *g, const float *S0, void *o,
+                      float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk, int64_t dv, int64_t chunk,
+                      lr_dtype io, void *workspace, size_t ws_bytes, lr_stream_t stream, bool async_) {
     int rc = validate_hgrn2(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io);
     if (rc != LR_OK) return rc;
     if (B == 0) return LR_OK;
@@ -727,7 +756,23 @@ extern "C" int lr_hgrn2_fwd_host(const void *q, const void *k, const void *v, co
     const HgHost a{B, H, dk, dv, chunk, io};
     const lr::HostJob j = hg_host_job(a, L, q, k, v, g, S0, o, S_final);
     if ((rc = host_ws_check(j, workspace, ws_bytes)) != LR_OK) return rc;
-    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), async_);
+}
+
+extern "C" int lr_hgrn2_fwd_host(const void *q, const void *k, const void *v, const void *g, const float *S0,
+                                 void *o, float *S_final, int64_t B, int64_t L, int64_t H, int64_t dk,
+                                 int64_t dv, int64_t chunk, lr_dtype io, void *workspace, size_t ws_bytes,
+                                 lr_stream_t stream) {
+    return hgrn2_host(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io, workspace, ws_bytes, stream,
+                      false);
+}
+
+extern "C" int lr_hgrn2_fwd_host_async(const void *q, const void *k, const void *v, const void *g,
+                                       const float *S0, void *o, float *S_final, int64_t B, int64_t L,
+                                       int64_t H, int64_t dk, int64_t dv, int64_t chunk, lr_dtype io,
+                                       void *workspace, size_t ws_bytes, lr_stream_t stream) {
+    return hgrn2_host(q, k, v, g, S0, o, S_final, B, L, H, dk, dv, chunk, io, workspace, ws_bytes, stream,
+                      true);
 }
 
 extern "C" size_t lr_minmax_scan_fwd_host_workspace_size(int64_t B, int64_t L, int64_t D, lr_dtype io) {
@@ -737,9 +782,9 @@ extern "C" size_t lr_minmax_scan_fwd_host_workspace_size(int64_t B, int64_t L, i
     return j.kernel_ws == SIZE_MAX ? SIZE_MAX : lr::host_workspace_bytes(j);
 }
 
-extern "C" int lr_minmax_scan_fwd_host(const void *r, const void *s, const float *x0, void *y, float *x_final,
-                                       int64_t B, int64_t L, int64_t D, lr_dtype io, void *workspace,
-                                       size_t ws_bytes, lr_stream_t stream) {
+static int minmax_host(const void *r, const void *s, const float *x0, void *y, float *x_final, int64_t B,
+                       int64_t L, int64_t D, lr_dtype io, void *workspace, size_t ws_bytes,
+                       lr_stream_t stream, bool async_) {
     int rc = validate_minmax(r, s, x0, y, x_final, B, L, D, io);
     if (rc != LR_OK) return rc;
     if (B == 0 || D == 0) return LR_OK;
@@ -750,5 +795,19 @@ extern "C" int lr_minmax_scan_fwd_host(const void *r, const void *s, const float
     const MmHost a{B, D, io};
     const lr::HostJob j = mm_host_job(a, L, r, s, x0, y, x_final);
     if ((rc = host_ws_check(j, workspace, ws_bytes)) != LR_OK) return rc;
-    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return lr::run_host_job(j, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream), async_);
 }
+
+extern "C" int lr_minmax_scan_fwd_host(const void *r, const void *s, const float *x0, void *y, float *x_final,
+                                       int64_t B, int64_t L, int64_t D, lr_dtype io, void *workspace,
+                                       size_t ws_bytes, lr_stream_t stream) {
+    return minmax_host(r, s, x0, y, x_final, B, L, D, io, workspace, ws_bytes, stream, false);
+}
+
+extern "C" int lr_minmax_scan_fwd_host_async(const void *r, const void *s, const float *x0, void *y,
+                                             float *x_final, int64_t B, int64_t L, int64_t D, lr_dtype io,
+                                             void *workspace, size_t ws_bytes, lr_stream_t stream) {
+    return minmax_host(r, s, x0, y, x_final, B, L, D, io, workspace, ws_bytes, stream, true);
+}
+
+extern "C" int lr_host_sync(void) { return lr::host_sync(); }

@@ -131,7 +131,7 @@ int64_t host_chunk_steps(int64_t B, int64_t L, size_t in_bytes_per_step) {
 
 size_t host_workspace_bytes(const HostJob &job) { return layout(job).total; }
 
-int run_host_job(const HostJob &j, void *workspace, size_t ws_bytes, cudaStream_t caller) {
+int run_host_job(const HostJob &j, void *workspace, size_t ws_bytes, cudaStream_t caller, bool async_) {
     const Layout lay = layout(j);
     if (workspace == nullptr || ws_bytes < lay.total) return LR_ERR_WORKSPACE;
     int dev = 0, max_pitch = 0;
@@ -200,6 +200,14 @@ int run_host_job(const HostJob &j, void *workspace, size_t ws_bytes, cudaStream_
     if (ok && rc == LR_OK && j.state_final != nullptr)
         ok = cudaMemcpyAsync(j.state_final, state[K & 1], j.state_bytes, cudaMemcpyDeviceToHost,
                              r->s_out) == cudaSuccess;
+    // the asynchronous form returns with the work queued: a later call's
+    // copies follow this call's on the same streams and overlap its last
+    // chunks; host_sync() waits for all of it, and the device-side status is
+    // read from the workspace afterwards
+    if (async_) {
+        if (rc != LR_OK) return rc;
+        return ok ? LR_OK : LR_ERR_CUDA;
+    }
     // nothing may still use the workspace or the host buffers on return
     const bool synced = cudaStreamSynchronize(r->s_in) == cudaSuccess &&
                         cudaStreamSynchronize(r->s_comp) == cudaSuccess &&
@@ -210,6 +218,17 @@ int run_host_job(const HostJob &j, void *workspace, size_t ws_bytes, cudaStream_
     int code = LR_OK;
     if (read_status(ws + lay.kws, r->s_comp, &code, false) != LR_OK) return LR_ERR_CUDA;
     return code;
+}
+
+int host_sync() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LR_ERR_CUDA;
+    HostRes *r = host_res(dev);
+    if (r == nullptr) return LR_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(r->mu);
+    const bool ok = cudaStreamSynchronize(r->s_in) == cudaSuccess && cudaStreamSynchronize(r->s_comp) == cudaSuccess &&
+                    cudaStreamSynchronize(r->s_out) == cudaSuccess;
+    return ok ? LR_OK : LR_ERR_CUDA;
 }
 
 }  // namespace lr

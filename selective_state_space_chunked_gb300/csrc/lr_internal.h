@@ -165,6 +165,11 @@ struct HostJob {
 int64_t host_chunk_steps(int64_t B, int64_t L, size_t in_bytes_per_step);
 extern int64_t g_host_chunk_override;   // lr_set_host_chunk_steps
 size_t host_workspace_bytes(const HostJob &job);
-int run_host_job(const HostJob &job, void *workspace, size_t ws_bytes, cudaStream_t caller);
+// async_: return once the work is queued (no synchronisation, the device-side
+// status is left in the workspace); host_sync() waits for every queued call
+// of the current device.
+int run_host_job(const HostJob &job, void *workspace, size_t ws_bytes, cudaStream_t caller,
+                 bool async_ = false);
+int host_sync();
 
 }  // namespace lr

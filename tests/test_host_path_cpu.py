@@ -71,3 +71,22 @@ def test_empty_sequence_copies_the_state_on_the_host(lr, with_h0):
         hf = np.full(shape, 7.0, dtype=np.float32)
         assert call(ptr(h0) if with_h0 else None, ptr(hf)) == lr.LR_OK
         np.testing.assert_array_equal(hf, h0 if with_h0 else np.zeros(shape, np.float32))
+
+
+def test_queued_host_entry_points_check_arguments_as_the_synchronous_ones(lr):
+    """The *_async forms share the synchronous forms' argument checks, which
+    return before anything is queued; the empty sequence copies the state on
+    the host without queueing anything either."""
+    assert lr.lr_rglru_scan_fwd_host_async(FAKE, FAKE, FAKE, FAKE, 8.0, None, FAKE, None, -1, 4, 8, 1,
+                                           FAKE, 1 << 20, None) == lr.LR_ERR_INVALID_ARG
+    assert lr.lr_selective_scan_fwd_host_async(FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None, FAKE, None,
+                                               1, 4, 8, 8, 1, 1, FAKE, 1 << 20, None) == lr.LR_ERR_UNSUPPORTED
+    assert lr.lr_minmax_scan_fwd_host_async(FAKE + 4, FAKE, None, FAKE, None, 1, 4, 8, 1, FAKE, 1 << 20,
+                                            None) == lr.LR_ERR_MISALIGNED
+    assert lr.lr_hgrn2_fwd_host_async(FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 4, 1, 513, 8, 64, 1,
+                                      FAKE, 1 << 20, None) == lr.LR_ERR_UNSUPPORTED
+    h0 = np.arange(16, dtype=np.float32).reshape(2, 8)
+    hf = np.zeros_like(h0)
+    assert lr.lr_rglru_scan_fwd_host_async(FAKE, FAKE, FAKE, FAKE, 8.0, ptr(h0), FAKE, ptr(hf), 2, 0, 8, 1,
+                                           None, 0, None) == lr.LR_OK
+    np.testing.assert_array_equal(hf, h0)

@@ -138,3 +138,42 @@ def test_host_path_calls_from_two_threads_match_sequential(lr, chunk):
     assert not errors, errors
     for (y, hf), (yr, hr) in zip(got, ref):
         assert torch.equal(y, yr) and torch.equal(hf, hr)
+
+
+def test_queued_host_calls_match_the_synchronous_calls(lr, chunk):
+    """RG-LRU, selective, HGRN2 and MinMax host-buffer calls queued with
+    ``sync_host=False`` (two with their own workspace, two with one the
+    binding allocates), then one ``host_sync()``: the calls overlap on the
+    library's streams and every output and final state matches the
+    synchronous call's (the same kernels over the same chunks); each call's
+    device status is clear."""
+    rg = pinned(wl.rglru_inputs(2, 333, 64, seed=41, io="bf16", with_h0=True))
+    se = pinned(wl.selective_inputs(2, 250, 64, seed=42, io="f32", with_h0=True))
+    hg = pinned(wl.hgrn2_inputs(1, 300, 2, 128, seed=43, io="bf16", with_S0=True))
+    g = torch.Generator().manual_seed(44)
+    mr = torch.randn(2, 333, 64, generator=g).to(torch.bfloat16).pin_memory()
+    ms = (torch.randn(2, 333, 64, generator=g) - 1.0).to(torch.bfloat16).pin_memory()
+    calls = [
+        lambda **kw: lr.rglru_scan(rg["x"], rg["r"], rg["i"], rg["a_log"], rg["c"], h0=rg["h0"], **kw),
+        lambda **kw: lr.selective_scan(se["x"], se["dt"], se["Bm"], se["Cm"], se["A_log"], z=se["z"],
+                                       Dskip=se["Dskip"], h0=se["h0"], **kw),
+        lambda **kw: lr.hgrn2(hg["q"], hg["k"], hg["v"], hg["g"], H=2, S0=0.1 * hg["S0"], **kw),
+        lambda **kw: lr.minmax_scan(mr, ms, **kw),
+    ]
+    sync = [c() for c in calls]
+    sizes = [lr.lr_rglru_scan_fwd_host_workspace_size(2, 333, 64, lr.LR_BF16),
+             lr.lr_selective_scan_fwd_host_workspace_size(2, 250, 64, 16, lr.LR_F32)]
+    wss = [torch.empty(n, dtype=torch.uint8, device="cuda") for n in sizes] + [None, None]
+    queued = []
+    for c, ws in zip(calls, wss):
+        queued.append(c(workspace=ws, sync_host=False))
+        if ws is None:
+            wss[len(queued) - 1] = lr._tls.ws   # the workspace the binding allocated for the call
+    lr.host_sync()
+    for ws in wss:
+        assert lr.status(ws) == 0
+    for (a, b), (ra, rb) in zip(queued, sync):
+        assert rel_err(a.float(), ra.float()) <= 1e-6 and rel_err(b, rb) <= 1e-6
+    assert torch.equal(queued[3][0], sync[3][0]) and torch.equal(queued[3][1], sync[3][1])
+    yr, hr = oracle.rglru_scan(rg["x"], rg["r"], rg["i"], rg["a_log"], rg["c"], h0=rg["h0"])
+    assert rel_err(queued[0][0].float(), yr) <= TOL["bf16"] and rel_err(queued[0][1], hr) <= TOL["bf16"]
