@@ -328,7 +328,7 @@ int lr_minmax_scan_fwd(const void *r, const void *s, const float *x0, void *y,
  * call, overlaps the scan.
  *
  * The library cuts the sequence into chunks of Lc time steps (a multiple of
- * 64, about 64 MB of inputs each) and runs each chunk with the matching
+ * 64, about 128 MB of inputs each) and runs each chunk with the matching
  * device entry point, the state carried from chunk to chunk on the device;
  * on three streams of its own it copies chunk k+1's inputs in while chunk k
  * runs and chunk k-1's outputs go out.  Arguments, layouts, requirements and
@@ -518,7 +518,7 @@ int64_t lr_set_selective_warmup(int64_t max_steps);
 /*
  * Tuning / test knob: the chunk length (time steps) of the host-buffer entry
  * points (lr_*_fwd_host); 0 restores the automatic choice (a multiple of 64
- * steps holding about 64 MB of inputs).  Any positive length is valid: chunk
+ * steps holding about 128 MB of inputs).  Any positive length is valid: chunk
  * boundaries need not fall on a kernel tile.  Process-wide; set it before
  * querying a host workspace size, which depends on it.  Returns the previous
  * setting.

@@ -123,7 +123,7 @@ int64_t g_host_chunk_override = 0;
 int64_t host_chunk_steps(int64_t B, int64_t L, size_t in_bytes_per_step) {
     if (g_host_chunk_override > 0) return g_host_chunk_override;
     const size_t per_step = size_t(B > 0 ? B : 1) * (in_bytes_per_step > 0 ? in_bytes_per_step : 1);
-    int64_t lc = int64_t((size_t(64) << 20) / per_step);
+    int64_t lc = int64_t((size_t(128) << 20) / per_step);
     lc = std::max<int64_t>(64, lc / 64 * 64);
     const int64_t l64 = std::max<int64_t>(64, (L + 63) / 64 * 64);
     return std::min(lc, l64);
