@@ -68,7 +68,7 @@ constexpr uint32_t E1 = SL + 16384;        // 2^(Lambda - m), fp32 [64 t][64 i] 
 constexpr uint32_t EM = E1 + 16384;        // 2^m [64]
 constexpr uint32_t GC = EM + 256;          // 2^Lambda_C [64]
 constexpr uint32_t TOT = GC + 256;         // quarter totals [4][64]
-constexpr uint32_t BAR = TOT + 1024;       // full, mma, done
+constexpr uint32_t BAR = TOT + 1024;       // full, mma, done, mma2
 constexpr uint32_t TSLOT = BAR + 32;
 constexpr uint32_t FLAGS = TSLOT + 16;     // [0] abort, [1] steep chunk seen
 constexpr uint32_t SMEM = FLAGS + 16;
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(hf::NT, 1)
     const int qcol = h * DK, vcol = h * DV + rb * RB;
     const int HV = H * DV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + BAR);
-    uint64_t *full = bars, *mma = bars + 1, *done = bars + 2;
+    uint64_t *full = bars, *mma = bars + 1, *done = bars + 2, *mma2 = bars + 3;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + TSLOT);
     volatile int *flags = reinterpret_cast<volatile int *>(sm + FLAGS);
     float *e1 = reinterpret_cast<float *>(sm + E1);
@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(hf::NT, 1)
     if (tid == 0) {
         mbar_init(full, 1);
         mbar_init(mma, 1);
-        mbar_init(done, 1);
+        mbar_init(done, 2);   // both MMA issuers (threads 0 and 32)
+        mbar_init(mma2, 2);   // dS, OI from thread 0; OX from thread 32
         flags[0] = 0;
         flags[1] = 0;
         fence_mbar_init();
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(hf::NT, 1)
     // epilogue / mask: rows t of the warp's quarter, column halves
     const int quarter = warp & 3;
     const int et = 16 * quarter + (lane & 15);
-    uint32_t mma_phase = 0;
+    uint32_t mma_phase = 0, mma2_phase = 0;
     bool ok = true;
     int pending = n_chunks > 0 ? 0 : -1;   // chunk whose Q, K copy is in flight
 
@@ -328,9 +329,12 @@ __global__ void __launch_bounds__(hf::NT, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
+        // dS^T = K^T V~' and OI = tril(P) V~ from thread 0, OX = Q S^T from
+        // thread 32 (a lane of another warp): two issuers halve the time the
+        // MMAs take to issue; each accumulator has one issuer, so its order
+        // of accumulation is unchanged
         if (tid == 0) {
             tc_fence_after();
-            // dS^T = K^T V~', OI = tril(P) V~, OX = Q S^T
 #pragma unroll
             for (int kk = 0; kk < C / 16; ++kk)
                 umma3(tmem + T_DS, umma_smem_desc(s_base + KH + kk * 2048, 8192, 1024),
@@ -342,6 +346,9 @@ __global__ void __launch_bounds__(hf::NT, 1)
                 umma3(tmem + T_OI, umma_smem_desc(s_base + PH + kk * 32, 16, 1024),
                       umma_smem_desc(s_base + PL + kk * 32, 16, 1024), umma_smem_desc(s_base + VH + kk * 32, 16, 1024),
                       umma_smem_desc(s_base + VL + kk * 32, 16, 1024), IDESC_OI, kk == 0);
+            umma_commit(mma2);
+        } else if (tid == 32) {
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
                 const uint32_t qoff = (kk >> 2) * 8192 + (kk & 3) * 32;
@@ -350,10 +357,10 @@ __global__ void __launch_bounds__(hf::NT, 1)
                       umma_smem_desc(s_base + SH + kk * 2048, 8192, 1024),
                       umma_smem_desc(s_base + SL + kk * 2048, 8192, 1024), IDESC_OX, kk == 0);
             }
-            umma_commit(mma);
+            umma_commit(mma2);
         }
-        if (!mbar_wait_bounded(mma, mma_phase & 1, timeout_ns)) flags[0] = 1;
-        ++mma_phase;
+        if (!mbar_wait_bounded(mma2, mma2_phase & 1, timeout_ns)) flags[0] = 1;
+        ++mma2_phase;
         tc_fence_after();
         if (__syncthreads_or(flags[0] != 0)) {
             ok = false;
@@ -403,8 +410,8 @@ __global__ void __launch_bounds__(hf::NT, 1)
     if (tid == 0 && flags[1] != 0) redo[bh] = sref.stamp;   // both blocks of the head may write it
     // nothing of this block's may still run on the tensor cores or land in its
     // shared memory when it exits
+    if (tid == 0 || tid == 32) umma_commit(done);   // each issuer's MMAs
     if (tid == 0) {
-        umma_commit(done);
         mbar_wait_bounded(done, 0, timeout_ns);
         if (pending >= 0) mbar_wait_bounded(full, pending & 1, timeout_ns);   // after a failed wait only
     }
